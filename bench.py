@@ -1,0 +1,496 @@
+"""Benchmark: the fused replicated fp8 KV-cache store on GB300.
+
+One step is one prefill's publication: 61 sparse-MLA layers, each storing
+4 requests x 3,584 tokens (14,336 rows) into 4 replicas of that layer's
+1,024-block cache, followed by that layer's device-epoch advance; the 122
+launches are captured in one CUDA graph and one step is one replay.  The
+workload follows "[Kernel][PCP] Publish replicated KV updates through
+PyTorch symmetric memory", Performance evidence (3,584-token prompts at
+concurrency 4, GLM-5.2's sparse layers) with seeded synthetic bf16 rows.
+
+Prints one JSON line: rows stored per second x replicas (whole job), the
+roofline of the store kernel against the measured HBM copy bandwidth, the
+end-to-end figure through the public API with host inputs, and the CPU
+oracle timed on the host as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from replication_token_warp_gb300 import build as kbuild  # noqa: E402
+from replication_token_warp_gb300 import inputs, kvpub  # noqa: E402
+
+METRIC = "KV rows stored/sec ×R replicas and achieved HBM GB/s vs GB300 peak"
+UNIT = "rows/s"
+WORKLOAD = "prefill_c4x3584_61layers"
+LAYERS = 61
+ROWS = 4 * 3584
+R = 4
+NUM_BLOCKS = 1024
+ROW_IN = 1408                  # bf16 bytes read per valid row
+ROW_OUT = 656 + 132            # bytes written per valid row and replica
+FALLBACK_HBM_GBS = 6800.0
+PROFILE = os.path.join(ROOT, "profiles", "store_mla_fp8_prefill_c4x3584.md")
+
+
+def store_bytes(num_tokens: int, num_valid: int, replicas: int) -> int:
+    """Algorithmic HBM bytes of one store launch: slots + rows read once +
+    788 bytes per valid row and replica written."""
+    return 8 * num_tokens + num_valid * (ROW_IN + ROW_OUT * replicas)
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(kbuild.CSRC)):
+        with open(os.path.join(kbuild.CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the kernel source as it stands (else None)."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu, self.period = gpu_index, period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4)
+                          if r[3][5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Spec:
+    """A benchmark workload: `layers` store launches per step, each on its
+    own inputs and caches (distinct buffers, so a step's working set is
+    larger than L2), every launch followed by an epoch advance."""
+
+    def __init__(self, name, layers, make, replicas, num_blocks, note):
+        self.name, self.layers, self.make = name, layers, make
+        self.replicas, self.num_blocks, self.note = replicas, num_blocks, note
+
+
+def _copy_of(index):
+    w = inputs.make(index)
+    return lambda layer: w
+
+
+def _stress(layer):
+    """128 requests x 1,024 tokens (131,072 rows) into 8,192-block caches:
+    one launch moves ~600 MB (~4.6x L2), so ncu's DRAM counters see the
+    writes; about 1.9 GB on the device."""
+    return inputs.prefill_batch(1000 + layer, 128, 1024, 8192)
+
+
+def _prefill_layer_fn():
+    slots = inputs.layer_slot_mapping()
+    return lambda layer: inputs.prefill_layer(layer, slots)
+
+
+SPECS = {
+    "prefill_c4x3584_61layers": lambda: Spec(
+        WORKLOAD, LAYERS, _prefill_layer_fn(), 4, 1024,
+        "61 layers, seeds 3+layer, one shared slot_mapping"),
+    "prefill_c16x1024": lambda: Spec(
+        "prefill_c16x1024", 8, _copy_of(2), 4, 4096,
+        "8 buffer copies of the c16 x 1024 batch per step"),
+    "capacity_706624": lambda: Spec(
+        "capacity_706624", 4, _copy_of(4), 4, 11041,
+        "4 buffer copies of the 706,624-slot capacity batch per step"),
+    "stress_131072": lambda: Spec(
+        "stress_131072", 1, _stress, 4, 8192,
+        "one 131,072-row launch (profiling case)"),
+}
+
+
+class Step:
+    """All layers resident in HBM: packed bf16 rows [T, 704] per layer
+    (latent | rope | Indexer-K as strided views), a slot_mapping and R
+    replica caches per layer, one epoch counter."""
+
+    def __init__(self, dev, spec: Spec):
+        self.dev, self.spec = dev, spec
+        L = spec.layers
+        ws = [spec.make(layer) for layer in range(L)]
+        T = ws[0].num_tokens
+        self.num_tokens = T
+        self.valid = [w.num_valid for w in ws]
+        host = torch.empty(L, T, 704, dtype=torch.bfloat16, pin_memory=True)
+        for layer, w in enumerate(ws):
+            row = np.concatenate([w.kv_latent, w.k_rope, w.index_k], axis=1)
+            host[layer].copy_(torch.from_numpy(row.view(np.int16)).view(torch.bfloat16))
+        self.host_rows = host
+        self.rows = host.to(dev)
+        self.host_slots = torch.from_numpy(np.stack([w.slot_mapping for w in ws])).pin_memory()
+        self.slots = self.host_slots.to(dev)
+        nb = spec.num_blocks
+        self.main = [[torch.full((nb * 64 * 656,), inputs.GUARD_BYTE, dtype=torch.uint8,
+                                 device=dev) for _ in range(spec.replicas)] for _ in range(L)]
+        self.idx = [[torch.full((nb * 8448,), inputs.GUARD_BYTE, dtype=torch.uint8,
+                                device=dev) for _ in range(spec.replicas)] for _ in range(L)]
+        self.epoch = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.invalid = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def views(self, layer):
+        x = self.rows[layer]
+        return x[:, :512], x[:, 512:576], x[:, 576:704]
+
+    def launch_layers(self, events=None):
+        for layer in range(self.spec.layers):
+            lat, rope, idx = self.views(layer)
+            if events is not None:
+                events[2 * layer].record()
+            kvpub.store_mla_fp8(lat, rope, idx, self.slots[layer], self.main[layer],
+                                self.idx[layer], self.spec.num_blocks,
+                                invalid_count=self.invalid)
+            if events is not None:
+                events[2 * layer + 1].record()
+            kvpub.epoch_advance(self.epoch)
+
+    def capture(self, timed_events: bool):
+        events = None
+        if timed_events:
+            try:
+                events = [torch.cuda.Event(enable_timing=True, external=True)
+                          for _ in range(2 * self.spec.layers)]
+            except TypeError:
+                events = None
+        self.launch_layers()                     # load kernels before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.launch_layers(events)
+        return g, events
+
+
+def time_graph(g, steps, warmup):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    start.record()
+    for _ in range(steps):
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    barrier()
+    return start.elapsed_time(end), t0, t1
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if torch.distributed.get_backend() == "nccl" else "cpu")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def e2e_measure(step: Step, steps: int, warmup: int):
+    """Through the public API with host inputs: every step copies the 61
+    layers' pinned host rows and the slot_mapping to the device, runs the
+    61 stores and epoch advances, and reads the epoch back to the host."""
+    dev = step.dev
+    host_epoch = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    h2d = step.host_rows.numel() * 2 + step.host_slots.numel() * 8
+    d2h = 8
+
+    def run_once():
+        step.rows.copy_(step.host_rows, non_blocking=True)
+        step.slots.copy_(step.host_slots, non_blocking=True)
+        step.launch_layers()
+        host_epoch.copy_(step.epoch, non_blocking=True)
+
+    for _ in range(warmup):
+        run_once()
+    torch.cuda.synchronize()
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        run_once()
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end), h2d, d2h, int(host_epoch.item())
+
+
+def cpu_baseline(budget_s: float):
+    """The oracle as it stands, single-threaded, over as many layers of the
+    same workload as fit in about budget_s seconds of oracle time (at least
+    one layer); input generation is outside the timed calls."""
+    import oracle
+    slots = inputs.layer_slot_mapping()
+    main, idx = oracle.new_caches(R, NUM_BLOCKS)
+    rows, layers, elapsed = 0, 0, 0.0
+    while layers < LAYERS and (layers == 0 or elapsed < budget_s):
+        w = inputs.prefill_layer(layers, slots)
+        t = time.perf_counter()
+        n, _ = oracle.store_mla_fp8(w.kv_latent, w.k_rope, w.index_k, w.slot_mapping, main, idx,
+                                    NUM_BLOCKS)
+        elapsed += time.perf_counter() - t
+        rows += n
+        layers += 1
+    return {"value": rows * R / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{layers} of {LAYERS} layers ({rows} rows x {R} replicas), "
+                      f"scalar C oracle, 1 thread, {elapsed:.1f} s",
+            "host_cpus": os.cpu_count()}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kbuild.build()
+    kvpub.lib()
+    spec = SPECS[args.workload]()
+    step = Step(dev, spec)
+    L, Rr = spec.layers, spec.replicas
+    g, events = step.capture(timed_events=True)
+    with ClockSampler(local) as clocks:
+        total_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
+    total_ms = max_over_ranks(total_ms)
+    ms_per_step = total_ms / args.steps
+    expected_epoch = L * (1 + args.warmup + args.steps)
+    epoch = int(step.epoch.item())
+    if epoch != expected_epoch:
+        raise RuntimeError(f"epoch {epoch} != {expected_epoch}: launches were lost")
+
+    rows_x_r = sum(step.valid) * Rr
+    value = world * rows_x_r / (ms_per_step / 1e3)
+    launch_bytes = [store_bytes(step.num_tokens, v, Rr) for v in step.valid]
+    per_launch = sum(launch_bytes) / L
+    peak, peak_kind = measured_peak()
+    if events is not None:
+        durs = [events[2 * k].elapsed_time(events[2 * k + 1]) for k in range(L)]
+        kernel_ms = sum(durs) / len(durs)
+        timing = f"CUDA events around each of the {L} store launches in the last timed replay"
+    else:
+        kernel_ms = ms_per_step / L
+        timing = f"step time / {L} (this torch cannot record events inside a graph)"
+    achieved = per_launch / (kernel_ms / 1e3) / 1e9
+    traffic = profiled_traffic() if spec.name == WORKLOAD else None
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": f"store_mla_fp8_kernel<{Rr}>",
+                "algorithmic_bytes": int(round(per_launch)),
+                "kernel_us": round(kernel_ms * 1e3, 2), "peak_source": f"{peak_kind} hbm_gbs",
+                "timing": timing}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 50))
+        e2e_ms, h2d, d2h, _ = e2e_measure(step, e2e_steps, max(1, min(args.warmup, 3)))
+        e2e_ms = max_over_ranks(e2e_ms)
+        e2e = {"value": world * rows_x_r / (e2e_ms / e2e_steps / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": spec.name, "layers": L, "rows_per_layer": step.num_tokens,
+                   "valid_rows_per_layer": step.valid[0], "replicas": Rr,
+                   "blocks_per_replica": spec.num_blocks, "launches_per_step": 2 * L,
+                   "graph": True, "parallelism": f"replicas only x{world}", "note": spec.note,
+                   "l2": "inputs larger than L2: one step touches "
+                         f"{sum(launch_bytes) / 1e9:.2f} GB",
+                   "hbm_gbs_step": round(sum(launch_bytes) / (ms_per_step / 1e3) / 1e9, 1)},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 2 * L * args.steps,
+        "clocks": clocks.summary(t0, t1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as it stands, on the same workload and metric."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    slots = inputs.layer_slot_mapping()
+    w = inputs.prefill_layer(0, slots)
+    main, idx = oracle.new_caches(R, NUM_BLOCKS)
+    # size each step so warmup + steps take about two minutes in total
+    t = time.perf_counter()
+    oracle.store_mla_fp8(w.kv_latent[:256], w.k_rope[:256], w.index_k[:256],
+                         w.slot_mapping[:256], main, idx, NUM_BLOCKS)
+    per_row = (time.perf_counter() - t) / 256
+    rows = int(min(ROWS, max(64, 120.0 / (args.steps + args.warmup) / per_row)))
+    sample = slice(0, rows)
+    valid = int(np.count_nonzero(w.slot_mapping[sample] >= 0))
+    call = (w.kv_latent[sample], w.k_rope[sample], w.index_k[sample], w.slot_mapping[sample],
+            main, idx, NUM_BLOCKS)
+    for _ in range(args.warmup):
+        oracle.store_mla_fp8(*call)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.store_mla_fp8(*call)
+    elapsed = time.perf_counter() - t
+    value = valid * R * args.steps / elapsed
+    desc = (f"{rows} of {ROWS} rows of layer 0 per step, scalar C oracle, 1 thread")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "layers": LAYERS, "rows_per_layer": ROWS,
+                      "replicas": R, "blocks_per_replica": NUM_BLOCKS},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline field")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=sorted(SPECS), default=WORKLOAD,
+                    help="the default is the measured line; the others are for "
+                         "per-workload roofline figures and ncu captures")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        run_ours(args)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

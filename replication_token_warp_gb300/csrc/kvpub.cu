@@ -1,0 +1,510 @@
+// libkvpub: the fused replicated fp8 KV-cache store and its companions,
+// hand-written for GB300 (sm_103a).  The C ABI is declared in kvpub.h.
+//
+// Direct publication ("[Kernel][PCP] Publish replicated KV updates through
+// PyTorch symmetric memory", Summary and the "THIS PR" diagram): one launch
+// reads each token row once, quantises it in registers and stores the final
+// bytes to all R replicas.  The work is HBM-bound (1408 bytes read and
+// 788 * R bytes written per row); no tensor cores, no shared memory.
+
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <atomic>
+
+#include "kvpub.h"
+#include "quant.cuh"
+
+namespace kvpub {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kThreads = kWarpsPerBlock * 32;
+constexpr unsigned long long kMaxPolls = KVPUB_MAX_POLLS;
+
+struct Replicas {
+    uint8_t *main[KVPUB_MAX_REPLICAS];
+    uint8_t *indexer[KVPUB_MAX_REPLICAS];
+};
+
+struct StoreArgs {
+    const uint16_t *latent;
+    const uint16_t *rope;
+    const uint16_t *index_k;
+    int64_t latent_stride;   // elements
+    int64_t rope_stride;
+    int64_t index_stride;
+    const int64_t *slot_mapping;
+    int64_t num_tokens;
+    int64_t num_slots;
+    unsigned long long *invalid_count;
+    Replicas rep;
+};
+
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream8(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st16(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st4(void *p, uint32_t v) {
+    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// One token row, quantised and stored to every replica.  All lanes of the
+// warp call this together (s is warp-uniform).
+template <int R>
+__device__ __forceinline__ void publish_row(const StoreArgs &a, int64_t t, int64_t s,
+                                            int lane) {
+    const uint8_t *lat = reinterpret_cast<const uint8_t *>(a.latent + t * a.latent_stride);
+    const uint4 x0 = ld_stream16(lat + 32 * lane);
+    const uint4 x1 = ld_stream16(lat + 32 * lane + 16);
+    const uint2 xi = ld_stream8(reinterpret_cast<const uint8_t *>(a.index_k + t * a.index_stride) +
+                                8 * lane);
+    uint4 tail = make_uint4(0u, 0u, 0u, 0u);
+    if (lane >= 1 && lane <= 8)
+        tail = ld_stream16(reinterpret_cast<const uint8_t *>(a.rope + t * a.rope_stride) +
+                           16 * (lane - 1));
+
+    // amax: latent tile (8 lanes) in the low half, Indexer-K (32 lanes) high.
+    uint32_t m_lat = absmax_bf16x2(absmax_bf16x2(x0.x, x0.y), absmax_bf16x2(x0.z, x0.w));
+    m_lat = __vmaxu2(m_lat, absmax_bf16x2(absmax_bf16x2(x1.x, x1.y), absmax_bf16x2(x1.z, x1.w)));
+    const uint32_t m_idx = halves_max(absmax_bf16x2(xi.x, xi.y));
+    uint32_t packed = halves_max(m_lat) | (m_idx << 16);
+    packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 1));
+    packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 2));
+    packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 4));
+    const float s_lat = tile_scale(packed & 0xffffu);
+    packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 8));
+    packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 16));
+    const float s_idx = tile_scale(packed >> 16);
+
+    const uint2 q0 = quant_bf16x8(x0, s_lat);
+    const uint2 q1 = quant_bf16x8(x1, s_lat);
+    const uint4 q_lat = make_uint4(q0.x, q0.y, q1.x, q1.y);
+    const uint32_t q_idx = quant_bf16x2(xi.x, s_idx) | (quant_bf16x2(xi.y, s_idx) << 16);
+
+    // lane 0 carries the 4 tile scales (row bytes 512..527); lanes 1..8
+    // carry the rope (bytes 528..655).
+    const float s1 = __shfl_sync(kFullMask, s_lat, 8);
+    const float s2 = __shfl_sync(kFullMask, s_lat, 16);
+    const float s3 = __shfl_sync(kFullMask, s_lat, 24);
+    if (lane == 0)
+        tail = make_uint4(__float_as_uint(s_lat), __float_as_uint(s1), __float_as_uint(s2),
+                          __float_as_uint(s3));
+
+    const int64_t main_off = s * KVPUB_MAIN_SLOT_BYTES;
+    const int64_t blk = s >> 6, off = s & 63;
+    const int64_t idx_off = blk * KVPUB_INDEXER_BLOCK_BYTES + off * KVPUB_INDEXER_DIM;
+    const int64_t idx_scale_off = blk * KVPUB_INDEXER_BLOCK_BYTES +
+                                  KVPUB_BLOCK_SIZE * KVPUB_INDEXER_DIM + off * 4;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        uint8_t *row = a.rep.main[r] + main_off;
+        st16(row + 16 * lane, q_lat);
+        if (lane <= 8) st16(row + 512 + 16 * lane, tail);
+        uint8_t *ib = a.rep.indexer[r];
+        st4(ib + idx_off + 4 * lane, q_idx);
+        if (lane == 0) st4(ib + idx_scale_off, __float_as_uint(s_idx));
+    }
+}
+
+// Grid-stride over token rows, one warp per row.
+template <int R>
+__device__ __forceinline__ void publish_rows(const StoreArgs &a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t t = warp; t < a.num_tokens; t += num_warps) {
+        const int64_t s = a.slot_mapping[t];
+        if (s < 0 || s >= a.num_slots) {
+            if (s != -1 && lane == 0 && a.invalid_count != nullptr)
+                atomicAdd(a.invalid_count, 1ull);
+            continue;
+        }
+        publish_row<R>(a, t, s, lane);
+    }
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads) store_mla_fp8_kernel(const StoreArgs a) {
+    publish_rows<R>(a);
+}
+
+__device__ __forceinline__ void release_add_epoch(unsigned long long *epoch) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(epoch) : "memory");
+}
+
+// Store, then the last block to finish publishes the epoch.
+template <int R>
+__global__ void __launch_bounds__(kThreads)
+store_mla_fp8_publish_kernel(const StoreArgs a, unsigned long long *epoch,
+                             unsigned int *done_count) {
+    publish_rows<R>(a);
+    __shared__ bool is_last;
+    __threadfence();                      // this thread's stores, GPU-wide
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned int prev = atomicAdd(done_count, 1u);
+        is_last = (prev == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (is_last && threadIdx.x == 0) {
+        __threadfence();                  // acquire every block's stores
+        atomicExch(done_count, 0u);       // ready for the next call / replay
+        release_add_epoch(epoch);
+    }
+}
+
+// Gather step of the unfused path: every token's bf16 row into one
+// 1408-byte workspace row (latent | rope | index_k).
+__global__ void __launch_bounds__(kThreads)
+gather_rows_kernel(const StoreArgs a, uint8_t *workspace) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t t = warp; t < a.num_tokens; t += num_warps) {
+        uint8_t *w = workspace + t * KVPUB_GATHER_ROW_BYTES;
+        const uint8_t *lat = reinterpret_cast<const uint8_t *>(a.latent + t * a.latent_stride);
+        const uint8_t *rope = reinterpret_cast<const uint8_t *>(a.rope + t * a.rope_stride);
+        const uint8_t *idx = reinterpret_cast<const uint8_t *>(a.index_k + t * a.index_stride);
+        // 88 chunks of 16 bytes: 64 latent, 8 rope, 16 Indexer-K.
+        for (int c = lane; c < 88; c += 32) {
+            const uint8_t *src = c < 64 ? lat + 16 * c
+                                : c < 72 ? rope + 16 * (c - 64)
+                                         : idx + 16 * (c - 72);
+            st16(w + 16 * c, ld_stream16(src));
+        }
+    }
+}
+
+__global__ void epoch_advance_kernel(unsigned long long *epoch) {
+    release_add_epoch(epoch);
+}
+
+__global__ void epoch_wait_kernel(const unsigned long long *epoch, unsigned long long target,
+                                  unsigned long long max_polls, unsigned int *status) {
+    unsigned int st = 1u;
+    for (unsigned long long i = 0; i < max_polls; ++i) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(epoch) : "memory");
+        if (v >= target) {
+            st = 0u;
+            break;
+        }
+        __nanosleep(64);
+    }
+    *status = st;
+}
+
+// ---------------------------------------------------------------- host side
+
+thread_local char g_last_error[512] = "";
+
+kvpub_status fail(kvpub_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kvpub_status ok() {
+    g_last_error[0] = '\0';
+    return KVPUB_OK;
+}
+
+bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+kvpub_status check_rows(const void *p, int64_t stride, int64_t dim, int64_t num_tokens,
+                        const char *name) {
+    if (p == nullptr) return fail(KVPUB_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, 16)) return fail(KVPUB_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+    if (stride < dim)
+        return fail(KVPUB_ERR_INVALID_ARG, "%s row stride %lld < %lld", name, (long long)stride,
+                    (long long)dim);
+    if (stride % 8 != 0)
+        return fail(KVPUB_ERR_ALIGNMENT, "%s row stride %lld is not a multiple of 8 elements",
+                    name, (long long)stride);
+    if (num_tokens > 0 && stride > INT64_MAX / 2 / num_tokens)
+        return fail(KVPUB_ERR_INVALID_ARG, "%s spans more than 2^62 bytes", name);
+    return KVPUB_OK;
+}
+
+struct Validated {
+    StoreArgs args;
+    int num_replicas;
+};
+
+kvpub_status validate(const void *kv_latent, int64_t latent_stride, const void *k_rope,
+                      int64_t rope_stride, const void *index_k, int64_t index_stride,
+                      const int64_t *slot_mapping, int64_t num_tokens,
+                      void *const *main_caches, void *const *indexer_caches, int num_replicas,
+                      int64_t num_blocks, int block_size, unsigned long long *invalid_count,
+                      Validated *out) {
+    if (num_replicas < 1) return fail(KVPUB_ERR_INVALID_ARG, "num_replicas %d < 1", num_replicas);
+    if (num_replicas > KVPUB_MAX_REPLICAS)
+        return fail(KVPUB_ERR_TOO_MANY_REPLICAS, "num_replicas %d > %d", num_replicas,
+                    KVPUB_MAX_REPLICAS);
+    if (block_size != KVPUB_BLOCK_SIZE)
+        return fail(KVPUB_ERR_INVALID_ARG, "block_size %d != %d", block_size, KVPUB_BLOCK_SIZE);
+    if (num_tokens < 0)
+        return fail(KVPUB_ERR_INVALID_ARG, "num_tokens %lld < 0", (long long)num_tokens);
+    if (num_blocks < 1 ||
+        num_blocks > INT64_MAX / (KVPUB_BLOCK_SIZE * (int64_t)KVPUB_MAIN_SLOT_BYTES))
+        return fail(KVPUB_ERR_INVALID_ARG, "num_blocks %lld out of range", (long long)num_blocks);
+    if (main_caches == nullptr || indexer_caches == nullptr)
+        return fail(KVPUB_ERR_INVALID_ARG, "cache pointer arrays are NULL");
+    if (invalid_count != nullptr && !aligned(invalid_count, 8))
+        return fail(KVPUB_ERR_ALIGNMENT, "invalid_count is not 8-byte aligned");
+    Replicas rep{};
+    for (int r = 0; r < num_replicas; ++r) {
+        if (main_caches[r] == nullptr || indexer_caches[r] == nullptr)
+            return fail(KVPUB_ERR_INVALID_ARG, "cache pointer of replica %d is NULL", r);
+        if (!aligned(main_caches[r], 16) || !aligned(indexer_caches[r], 16))
+            return fail(KVPUB_ERR_ALIGNMENT, "cache of replica %d is not 16-byte aligned", r);
+        rep.main[r] = static_cast<uint8_t *>(main_caches[r]);
+        rep.indexer[r] = static_cast<uint8_t *>(indexer_caches[r]);
+    }
+    if (num_tokens > 0) {
+        kvpub_status st;
+        if ((st = check_rows(kv_latent, latent_stride, KVPUB_LATENT_DIM, num_tokens,
+                             "kv_latent")) != KVPUB_OK)
+            return st;
+        if ((st = check_rows(k_rope, rope_stride, KVPUB_ROPE_DIM, num_tokens, "k_rope")) !=
+            KVPUB_OK)
+            return st;
+        if ((st = check_rows(index_k, index_stride, KVPUB_INDEXER_DIM, num_tokens,
+                             "index_k")) != KVPUB_OK)
+            return st;
+        if (slot_mapping == nullptr) return fail(KVPUB_ERR_INVALID_ARG, "slot_mapping is NULL");
+        if (!aligned(slot_mapping, 8))
+            return fail(KVPUB_ERR_ALIGNMENT, "slot_mapping is not 8-byte aligned");
+    }
+    out->args.latent = static_cast<const uint16_t *>(kv_latent);
+    out->args.rope = static_cast<const uint16_t *>(k_rope);
+    out->args.index_k = static_cast<const uint16_t *>(index_k);
+    out->args.latent_stride = latent_stride;
+    out->args.rope_stride = rope_stride;
+    out->args.index_stride = index_stride;
+    out->args.slot_mapping = slot_mapping;
+    out->args.num_tokens = num_tokens;
+    out->args.num_slots = num_blocks * KVPUB_BLOCK_SIZE;
+    out->args.invalid_count = invalid_count;
+    out->args.rep = rep;
+    out->num_replicas = num_replicas;
+    return KVPUB_OK;
+}
+
+// Resident blocks per SM for each kernel, times the SM count, per device.
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::atomic<int> sm_count{0};
+};
+DeviceInfo g_devices[kMaxDevices];
+
+kvpub_status sm_count(int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(KVPUB_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(KVPUB_ERR_CUDA, "device %d out of range", dev);
+    int n = g_devices[dev].sm_count.load(std::memory_order_relaxed);
+    if (n == 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return fail(KVPUB_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        g_devices[dev].sm_count.store(n, std::memory_order_relaxed);
+    }
+    *out = n;
+    return KVPUB_OK;
+}
+
+// Blocks for a grid-stride pass over num_tokens rows: enough to give every
+// row a warp, capped at kBlocksPerSm resident waves.
+constexpr int kBlocksPerSm = 8;
+
+kvpub_status grid_for(int64_t num_tokens, int *grid) {
+    int sms = 0;
+    kvpub_status st = sm_count(&sms);
+    if (st != KVPUB_OK) return st;
+    int64_t want = (num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    int64_t cap = static_cast<int64_t>(sms) * kBlocksPerSm;
+    if (want > cap) want = cap;
+    if (want < 1) want = 1;
+    *grid = static_cast<int>(want);
+    return KVPUB_OK;
+}
+
+kvpub_status launched(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(KVPUB_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+template <template <int> class Launch, typename... Args>
+void dispatch_replicas(int r, Args &&...args) {
+    switch (r) {
+        case 1: Launch<1>::go(args...); break;
+        case 2: Launch<2>::go(args...); break;
+        case 3: Launch<3>::go(args...); break;
+        case 4: Launch<4>::go(args...); break;
+        case 5: Launch<5>::go(args...); break;
+        case 6: Launch<6>::go(args...); break;
+        case 7: Launch<7>::go(args...); break;
+        default: Launch<8>::go(args...); break;
+    }
+}
+
+template <int R>
+struct LaunchStore {
+    static void go(int grid, cudaStream_t stream, const StoreArgs &a) {
+        store_mla_fp8_kernel<R><<<grid, kThreads, 0, stream>>>(a);
+    }
+};
+
+template <int R>
+struct LaunchPublish {
+    static void go(int grid, cudaStream_t stream, const StoreArgs &a, unsigned long long *epoch,
+                   unsigned int *done) {
+        store_mla_fp8_publish_kernel<R><<<grid, kThreads, 0, stream>>>(a, epoch, done);
+    }
+};
+
+}  // namespace
+}  // namespace kvpub
+
+using namespace kvpub;
+
+extern "C" kvpub_status kvpub_store_mla_fp8(
+    const void *kv_latent, int64_t latent_stride, const void *k_rope, int64_t rope_stride,
+    const void *index_k, int64_t index_stride, const int64_t *slot_mapping, int64_t num_tokens,
+    void *const *main_caches, void *const *indexer_caches, int num_replicas, int64_t num_blocks,
+    int block_size, unsigned long long *invalid_count, kvpub_stream_t stream) {
+    Validated v;
+    kvpub_status st = validate(kv_latent, latent_stride, k_rope, rope_stride, index_k,
+                               index_stride, slot_mapping, num_tokens, main_caches,
+                               indexer_caches, num_replicas, num_blocks, block_size,
+                               invalid_count, &v);
+    if (st != KVPUB_OK) return st;
+    if (num_tokens == 0) return ok();
+    int grid = 0;
+    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
+    (void)cudaGetLastError();
+    dispatch_replicas<LaunchStore>(v.num_replicas, grid, (cudaStream_t)stream, v.args);
+    return launched("store_mla_fp8");
+}
+
+extern "C" kvpub_status kvpub_store_mla_fp8_publish(
+    const void *kv_latent, int64_t latent_stride, const void *k_rope, int64_t rope_stride,
+    const void *index_k, int64_t index_stride, const int64_t *slot_mapping, int64_t num_tokens,
+    void *const *main_caches, void *const *indexer_caches, int num_replicas, int64_t num_blocks,
+    int block_size, unsigned long long *invalid_count, unsigned long long *epoch,
+    unsigned int *done_count, kvpub_stream_t stream) {
+    Validated v;
+    kvpub_status st = validate(kv_latent, latent_stride, k_rope, rope_stride, index_k,
+                               index_stride, slot_mapping, num_tokens, main_caches,
+                               indexer_caches, num_replicas, num_blocks, block_size,
+                               invalid_count, &v);
+    if (st != KVPUB_OK) return st;
+    if (epoch == nullptr || done_count == nullptr)
+        return fail(KVPUB_ERR_INVALID_ARG, "epoch or done_count is NULL");
+    if (!aligned(epoch, 8) || !aligned(done_count, 4))
+        return fail(KVPUB_ERR_ALIGNMENT, "epoch or done_count is misaligned");
+    int grid = 0;
+    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
+    (void)cudaGetLastError();
+    dispatch_replicas<LaunchPublish>(v.num_replicas, grid, (cudaStream_t)stream, v.args, epoch,
+                                     done_count);
+    return launched("store_mla_fp8_publish");
+}
+
+extern "C" size_t kvpub_gather_workspace_bytes(int64_t num_tokens) {
+    if (num_tokens <= 0) return 0;
+    return static_cast<size_t>(num_tokens) * KVPUB_GATHER_ROW_BYTES;
+}
+
+extern "C" kvpub_status kvpub_gather_insert(
+    const void *kv_latent, int64_t latent_stride, const void *k_rope, int64_t rope_stride,
+    const void *index_k, int64_t index_stride, const int64_t *slot_mapping, int64_t num_tokens,
+    void *const *main_caches, void *const *indexer_caches, int num_replicas, int64_t num_blocks,
+    int block_size, unsigned long long *invalid_count, void *workspace, size_t workspace_bytes,
+    kvpub_stream_t stream) {
+    Validated v;
+    kvpub_status st = validate(kv_latent, latent_stride, k_rope, rope_stride, index_k,
+                               index_stride, slot_mapping, num_tokens, main_caches,
+                               indexer_caches, num_replicas, num_blocks, block_size,
+                               invalid_count, &v);
+    if (st != KVPUB_OK) return st;
+    if (num_tokens == 0) return ok();
+    if (workspace == nullptr) return fail(KVPUB_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(workspace, 16))
+        return fail(KVPUB_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
+    if (workspace_bytes < kvpub_gather_workspace_bytes(num_tokens))
+        return fail(KVPUB_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", workspace_bytes,
+                    kvpub_gather_workspace_bytes(num_tokens));
+    int grid = 0;
+    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    (void)cudaGetLastError();
+    gather_rows_kernel<<<grid, kThreads, 0, s>>>(v.args, ws);
+    if ((st = launched("gather_rows")) != KVPUB_OK) return st;
+    // Insert: each replica quantises the gathered rows on its own.
+    StoreArgs ins = v.args;
+    const uint16_t *w16 = reinterpret_cast<const uint16_t *>(ws);
+    ins.latent = w16;
+    ins.rope = w16 + KVPUB_LATENT_DIM;
+    ins.index_k = w16 + KVPUB_LATENT_DIM + KVPUB_ROPE_DIM;
+    ins.latent_stride = ins.rope_stride = ins.index_stride = KVPUB_GATHER_ROW_BYTES / 2;
+    for (int r = 0; r < v.num_replicas; ++r) {
+        ins.rep = Replicas{};
+        ins.rep.main[0] = v.args.rep.main[r];
+        ins.rep.indexer[0] = v.args.rep.indexer[r];
+        ins.invalid_count = (r == 0) ? v.args.invalid_count : nullptr;
+        store_mla_fp8_kernel<1><<<grid, kThreads, 0, s>>>(ins);
+        if ((st = launched("insert_rows")) != KVPUB_OK) return st;
+    }
+    return ok();
+}
+
+extern "C" kvpub_status kvpub_epoch_advance(unsigned long long *epoch, kvpub_stream_t stream) {
+    if (epoch == nullptr) return fail(KVPUB_ERR_INVALID_ARG, "epoch is NULL");
+    if (!aligned(epoch, 8)) return fail(KVPUB_ERR_ALIGNMENT, "epoch is not 8-byte aligned");
+    (void)cudaGetLastError();
+    epoch_advance_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(epoch);
+    return launched("epoch_advance");
+}
+
+extern "C" kvpub_status kvpub_epoch_wait(const unsigned long long *epoch,
+                                         unsigned long long target,
+                                         unsigned long long max_polls, unsigned int *status,
+                                         kvpub_stream_t stream) {
+    if (epoch == nullptr || status == nullptr)
+        return fail(KVPUB_ERR_INVALID_ARG, "epoch or status is NULL");
+    if (!aligned(epoch, 8) || !aligned(status, 4))
+        return fail(KVPUB_ERR_ALIGNMENT, "epoch or status is misaligned");
+    if (max_polls < 1 || max_polls > kMaxPolls)
+        return fail(KVPUB_ERR_INVALID_ARG, "max_polls %llu outside [1, %llu]", max_polls,
+                    kMaxPolls);
+    (void)cudaGetLastError();
+    epoch_wait_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(epoch, target, max_polls, status);
+    return launched("epoch_wait");
+}
+
+extern "C" const char *kvpub_last_error(void) { return g_last_error; }

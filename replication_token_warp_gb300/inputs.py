@@ -222,6 +222,19 @@ def make(index: int, layer: int = 0) -> Workload:
     raise ValueError(f"no workload {index}")
 
 
+def prefill_batch(seed: int, num_requests: int, tokens_per_request: int, num_blocks: int,
+                  num_replicas: int = 4) -> Workload:
+    """A generic prefill batch: outlier-channel rows, each request filling a
+    contiguous token run in its own randomly permuted blocks."""
+    g = _gen(seed)
+    T = num_requests * tokens_per_request
+    lat, rope, idx = _rows_with_outlier_channels(g, T)
+    slots = _prefill_slots(g, num_requests, tokens_per_request, num_blocks)
+    return Workload(f"prefill(seed={seed},{num_requests}x{tokens_per_request})",
+                    _bf16_bits(lat), _bf16_bits(rope), _bf16_bits(idx), slots.numpy().copy(),
+                    int(num_replicas), int(num_blocks))
+
+
 def random_rows(seed: int, num_tokens: int, num_blocks: int, num_replicas: int = 1,
                 pad_fraction: float = 0.0, scale: float = 1.0) -> Workload:
     """A generic seeded workload: N(0, scale^2) rows, distinct random slots."""

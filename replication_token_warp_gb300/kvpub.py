@@ -1,0 +1,209 @@
+"""ctypes binding of libkvpub (argument marshalling only).
+
+Every operation runs in the CUDA library: these wrappers take torch CUDA
+tensors, check their shapes (the C ABI cannot see sizes), pass raw device
+pointers and the current torch stream, and raise ``KvpubError`` on a
+non-zero status.  There is no fallback: if the library is not built, the
+first call raises.
+
+Names follow the C ABI in include/kvpub.h: ``store_mla_fp8`` (fused direct
+publication into every replica), ``store_mla_fp8_publish`` (the same store
+plus the device-epoch advance, one launch), ``gather_insert`` (the unfused
+gather-then-insert path), ``epoch_advance`` and ``epoch_wait``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+LATENT_DIM = 512
+ROPE_DIM = 64
+INDEXER_DIM = 128
+BLOCK_SIZE = 64
+MAIN_SLOT_BYTES = 656
+INDEXER_BLOCK_BYTES = BLOCK_SIZE * 132
+GATHER_ROW_BYTES = 1408
+MAX_REPLICAS = 8
+MAX_POLLS = 1 << 24
+
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "TOO_MANY_REPLICAS", 4: "CUDA",
+          5: "WORKSPACE"}
+
+
+class KvpubError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"kvpub {STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_STORE_ARGS = [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+               ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.c_int, _i64, ctypes.c_int,
+               _vp]
+
+SIGNATURES = {
+    "kvpub_store_mla_fp8": (_STORE_ARGS + [_vp], ctypes.c_int),
+    "kvpub_store_mla_fp8_publish": (_STORE_ARGS + [_vp, _vp, _vp], ctypes.c_int),
+    "kvpub_gather_workspace_bytes": ([_i64], ctypes.c_size_t),
+    "kvpub_gather_insert": (_STORE_ARGS + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "kvpub_epoch_advance": ([_vp, _vp], ctypes.c_int),
+    "kvpub_epoch_wait": ([_vp, ctypes.c_uint64, ctypes.c_uint64, _vp, _vp], ctypes.c_int),
+    "kvpub_last_error": ([], ctypes.c_char_p),
+}
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with __graft_entry__.build() "
+                    "(there is no fallback implementation)")
+            handle = ctypes.CDLL(path)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+        return _lib
+
+
+def last_error() -> str:
+    return lib().kvpub_last_error().decode()
+
+
+def check(status: int) -> None:
+    if status != 0:
+        raise KvpubError(status, last_error())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _rows(x: torch.Tensor, dim: int, T: int, name: str):
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError(f"{name}: expected a 2-D bf16 CUDA tensor")
+    if x.stride(1) != 1 or x.shape[1] < dim or x.shape[0] < T:
+        raise ValueError(f"{name}: expected [>= {T}, >= {dim}] rows with unit inner stride")
+    return x.data_ptr(), x.stride(0)
+
+
+def _ptr_array(ts):
+    arr = (_vp * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def _caches(main_caches, indexer_caches, num_blocks):
+    if len(main_caches) != len(indexer_caches):
+        raise ValueError("need as many Indexer caches as Main caches")
+    for c in list(main_caches) + list(indexer_caches):
+        if not c.is_cuda or c.dtype != torch.uint8 or not c.is_contiguous():
+            raise ValueError("caches are contiguous uint8 CUDA tensors")
+    if num_blocks is None:
+        num_blocks = main_caches[0].numel() // (BLOCK_SIZE * MAIN_SLOT_BYTES)
+    for m, ix in zip(main_caches, indexer_caches):
+        if (m.numel() < num_blocks * BLOCK_SIZE * MAIN_SLOT_BYTES
+                or ix.numel() < num_blocks * INDEXER_BLOCK_BYTES):
+            raise ValueError(f"a cache is smaller than {num_blocks} blocks")
+    return _ptr_array(main_caches), _ptr_array(indexer_caches), int(num_blocks)
+
+
+def _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                num_blocks, invalid_count):
+    if slot_mapping.dtype != torch.int64 or slot_mapping.dim() != 1 or not slot_mapping.is_cuda:
+        raise ValueError("slot_mapping: expected a 1-D int64 CUDA tensor")
+    if not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous")
+    T = slot_mapping.shape[0]
+    lp, ls = _rows(kv_latent, LATENT_DIM, T, "kv_latent")
+    rp, rs = _rows(k_rope, ROPE_DIM, T, "k_rope")
+    ip, is_ = _rows(index_k, INDEXER_DIM, T, "index_k")
+    mains, idxs, nb = _caches(main_caches, indexer_caches, num_blocks)
+    cnt = None
+    if invalid_count is not None:
+        if invalid_count.dtype not in (torch.int64, torch.uint64) or not invalid_count.is_cuda:
+            raise ValueError("invalid_count: expected an int64 CUDA tensor")
+        cnt = invalid_count.data_ptr()
+    return [lp, ls, rp, rs, ip, is_, slot_mapping.data_ptr(), T, mains, idxs,
+            len(main_caches), nb, BLOCK_SIZE, cnt]
+
+
+def store_mla_fp8(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                  num_blocks=None, invalid_count=None, stream=None) -> None:
+    """Fused direct publication of every token row into all replicas."""
+    args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                       num_blocks, invalid_count)
+    check(lib().kvpub_store_mla_fp8(*args, _stream_handle(stream)))
+
+
+def store_mla_fp8_publish(kv_latent, k_rope, index_k, slot_mapping, main_caches,
+                          indexer_caches, epoch, done_count, num_blocks=None,
+                          invalid_count=None, stream=None) -> None:
+    """Fused publication plus the device-epoch advance, in one launch."""
+    args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                       num_blocks, invalid_count)
+    _counter(epoch, (torch.int64, torch.uint64), "epoch")
+    _counter(done_count, (torch.int32, torch.uint32), "done_count")
+    check(lib().kvpub_store_mla_fp8_publish(*args, epoch.data_ptr(), done_count.data_ptr(),
+                                            _stream_handle(stream)))
+
+
+def gather_workspace_bytes(num_tokens: int) -> int:
+    return int(lib().kvpub_gather_workspace_bytes(int(num_tokens)))
+
+
+def gather_insert(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                  workspace, num_blocks=None, invalid_count=None, stream=None) -> None:
+    """The unfused path: gather every row, then one insert launch per replica."""
+    args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                       num_blocks, invalid_count)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace: expected a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    check(lib().kvpub_gather_insert(*args, workspace.data_ptr(), nbytes,
+                                    _stream_handle(stream)))
+
+
+def _counter(t, dtypes, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in dtypes or t.numel() < 1:
+        raise ValueError(f"{name}: expected a CUDA tensor of {dtypes}")
+
+
+def epoch_advance(epoch: torch.Tensor, stream=None) -> None:
+    """Release all earlier stores on the stream, then add 1 to ``epoch``."""
+    _counter(epoch, (torch.int64, torch.uint64), "epoch")
+    check(lib().kvpub_epoch_advance(epoch.data_ptr(), _stream_handle(stream)))
+
+
+def epoch_wait(epoch: torch.Tensor, target: int, max_polls: int, status: torch.Tensor,
+               stream=None) -> None:
+    """Bounded acquire-wait until ``epoch >= target``; writes 0 (ok) / 1 (timeout)."""
+    _counter(epoch, (torch.int64, torch.uint64), "epoch")
+    _counter(status, (torch.int32, torch.uint32), "status")
+    check(lib().kvpub_epoch_wait(epoch.data_ptr(), int(target), int(max_polls),
+                                 status.data_ptr(), _stream_handle(stream)))

@@ -1,0 +1,113 @@
+"""The 61-layer prefill (4 requests x 3,584 tokens per layer, 4 replicas, a
+separate 1,024-block cache per layer) captured in one CUDA graph and
+replayed 10 times.
+
+The device epoch must advance on every replay ("[Perf][PCP] Fuse direct-KV
+publication fence", Motivation: a host-side epoch cannot advance inside a
+replayed graph; its summary: the replay test checks the epoch on every
+replay).  After the replays, every layer's four replicas must equal the
+oracle byte for byte, red zones included.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import Caches, assert_matches_oracle, bf16, oracle_caches
+from replication_token_warp_gb300 import build as kbuild
+from replication_token_warp_gb300 import inputs, kvpub
+
+pytestmark = pytest.mark.gpu
+
+LAYERS = 61
+REPLAYS = 10
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_device):
+    kbuild.build()
+    kvpub.lib()
+    return cuda_device
+
+
+@pytest.fixture(scope="module")
+def layers():
+    slots = inputs.layer_slot_mapping()
+    return slots, [inputs.prefill_layer(layer, slots) for layer in range(LAYERS)]
+
+
+def _device_layers(layers, dev):
+    slots, ws = layers
+    d_slots = torch.from_numpy(slots).to(dev)
+    xs = [(bf16(w.kv_latent, dev), bf16(w.k_rope, dev), bf16(w.index_k, dev)) for w in ws]
+    caches = [Caches(4, 1024, inputs.GUARD_BYTE, dev) for _ in range(LAYERS)]
+    return d_slots, xs, caches
+
+
+def _check_epoch_per_replay(g, epoch, per_replay):
+    start = int(epoch.item())
+    for k in range(1, REPLAYS + 1):
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(epoch.item()) == start + k * per_replay
+
+
+@pytest.mark.parametrize("variant", ["store_then_advance", "fused_publish"])
+def test_graph_replay_advances_epoch_and_matches_oracle(dev, layers, variant):
+    d_slots, xs, caches = _device_layers(layers, dev)
+    epoch = torch.zeros(1, dtype=torch.int64, device=dev)
+    done = torch.zeros(1, dtype=torch.int32, device=dev)
+    scratch_epoch = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def step(ep):
+        for layer in range(LAYERS):
+            lat, rope, idx = xs[layer]
+            c = caches[layer]
+            if variant == "store_then_advance":
+                kvpub.store_mla_fp8(lat, rope, idx, d_slots, c.main, c.idx)
+                kvpub.epoch_advance(ep)
+            else:
+                kvpub.store_mla_fp8_publish(lat, rope, idx, d_slots, c.main, c.idx, ep, done)
+
+    # one eager pass loads the kernels before capture (the store is idempotent)
+    step(scratch_epoch)
+    torch.cuda.synchronize()
+    assert int(scratch_epoch.item()) == LAYERS
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(epoch)
+    torch.cuda.synchronize()
+    assert int(epoch.item()) == 0              # capture runs nothing
+    _check_epoch_per_replay(g, epoch, LAYERS)
+    assert int(epoch.item()) == LAYERS * REPLAYS == 610
+    assert int(done.item()) == 0
+
+    check = range(LAYERS) if variant == "store_then_advance" else (0, 30, 60)
+    _, ws = layers
+    for layer in check:
+        want_main, want_idx, _, _ = oracle_caches(ws[layer])
+        assert_matches_oracle(caches[layer], want_main, want_idx)
+    del caches, xs
+    torch.cuda.empty_cache()
+
+
+def test_separate_epoch_lanes_in_one_graph(dev):
+    """Two epoch counters (two lanes) advanced in an interleaved order inside
+    one graph keep separate counts on every replay ("[Kernel][PCP] Publish
+    replicated KV updates through PyTorch symmetric memory", Design: the
+    device-epoch barrier supports separate DBO lanes)."""
+    lanes = torch.zeros(2, dtype=torch.int64, device=dev)
+    kvpub.epoch_advance(lanes[0:1])            # load the kernel
+    torch.cuda.synchronize()
+    lanes.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for k in range(7):
+            kvpub.epoch_advance(lanes[0:1])
+            if k % 2 == 0:
+                kvpub.epoch_advance(lanes[1:2])
+    for k in range(1, 6):
+        g.replay()
+        torch.cuda.synchronize()
+        assert lanes.tolist() == [7 * k, 4 * k]
