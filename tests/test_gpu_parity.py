@@ -250,7 +250,7 @@ def test_failures_change_nothing(dev):
     idxs = (ctypes.c_void_p * 1)(c.idx[0].data_ptr())
     base = [x.lat.data_ptr(), 512, x.rope.data_ptr(), 64, x.idx.data_ptr(), 128,
             x.slots.data_ptr(), w.num_tokens, mains, idxs, 1, w.num_blocks, 64, None]
-    bad = [(0, x.lat.data_ptr() + 2, 2), (1, 520, 2), (10, 0, 1), (10, 9, 3), (12, 16, 1),
+    bad = [(0, x.lat.data_ptr() + 2, 2), (1, 516, 2), (1, 504, 1), (10, 0, 1), (10, 9, 3), (12, 16, 1),
            (7, -5, 1), (13, x.slots.data_ptr() + 4, 2)]
     for i, v, st in bad:
         args = list(base)
