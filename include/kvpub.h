@@ -83,6 +83,7 @@ typedef enum {
 #define KVPUB_INDEXER_BLOCK_BYTES (KVPUB_BLOCK_SIZE * KVPUB_INDEXER_SLOT_BYTES)
 #define KVPUB_GATHER_ROW_BYTES 1408  /* (512 + 64 + 128) bf16 */
 #define KVPUB_MAX_POLLS (1ull << 24)
+#define KVPUB_STATIC_GATHER_MAX_TOKENS 4096
 
 /*
  * Fused direct publication. One launch stores every token's final Main-KV
@@ -177,6 +178,42 @@ kvpub_status kvpub_gather_insert(
     int64_t num_blocks, int block_size,
     unsigned long long *invalid_count,
     void *workspace, size_t workspace_bytes, kvpub_stream_t stream);
+
+/*
+ * Allocation-free gather-then-insert. It has no counterpart on the pages: it
+ * is kvpub_gather_insert for callers that cannot allocate device memory. Such
+ * callers include:
+ *  - a serving loop whose device memory is planned and reserved once at
+ *    start-up, so that nothing may be allocated while requests run;
+ *  - a plugin inside another runtime that owns all device memory;
+ *  - code on a latency-critical path, where cudaMalloc may synchronise the
+ *    device and stall every other stream.
+ * Its bytes equal kvpub_gather_insert's. The only difference is the
+ * workspace: a fixed array of KVPUB_STATIC_GATHER_MAX_TOKENS rows of 1408
+ * bytes (5.5 MiB) inside this library, not caller memory. Every GPU that
+ * loads the library holds that array until the process exits.
+ *
+ *  - num_tokens above KVPUB_STATIC_GATHER_MAX_TOKENS gives
+ *    KVPUB_ERR_WORKSPACE, and nothing is launched.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current, and keeps it for later calls. Make that first call
+ *    before any stream capture on the device.
+ *  - Every call uses the same array. Calls that can overlap on the GPU (on
+ *    different streams, or issued from several threads without ordering)
+ *    race on it and corrupt each other's rows. Issue them on one stream.
+ *  - No element of the array needs to start at zero. Each call writes every
+ *    workspace row before it reads it.
+ *  - It calls no cudaMalloc, no cudaFree and no allocating library routine.
+ * Other arguments, and the failure statuses, are as in kvpub_gather_insert.
+ */
+kvpub_status kvpub_gather_insert_noalloc(
+    const void *kv_latent, int64_t latent_stride,
+    const void *k_rope, int64_t rope_stride,
+    const void *index_k, int64_t index_stride,
+    const int64_t *slot_mapping, int64_t num_tokens,
+    void *const *main_caches, void *const *indexer_caches, int num_replicas,
+    int64_t num_blocks, int block_size,
+    unsigned long long *invalid_count, kvpub_stream_t stream);
 
 /*
  * Device-resident publication epoch: one single-thread launch. It makes

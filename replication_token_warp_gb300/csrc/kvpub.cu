@@ -508,3 +508,86 @@ extern "C" kvpub_status kvpub_epoch_wait(const unsigned long long *epoch,
 }
 
 extern "C" const char *kvpub_last_error(void) { return g_last_error; }
+
+// ------------------------------------------- allocation-free gather-insert
+//
+// kvpub_gather_insert with its workspace in a fixed array inside this
+// library instead of caller memory, for callers that cannot allocate device
+// memory.  Every GPU that loads the library holds the array
+// (KVPUB_STATIC_GATHER_MAX_TOKENS rows of 1408 bytes, 5.5 MiB) until the
+// process exits.  Host code cannot use the array's name as a device address:
+// the first call on each device looks the address up with that device
+// current and caches it.
+
+static __device__ __align__(256) uint8_t
+    g_static_gather_workspace[KVPUB_STATIC_GATHER_MAX_TOKENS * KVPUB_GATHER_ROW_BYTES];
+
+namespace kvpub {
+namespace {
+
+std::atomic<uint8_t *> g_static_workspace_addr[kMaxDevices];
+
+kvpub_status static_gather_workspace(uint8_t **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(KVPUB_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(KVPUB_ERR_CUDA, "device %d out of range", dev);
+    uint8_t *p = g_static_workspace_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_static_gather_workspace);
+        if (e != cudaSuccess || addr == nullptr)
+            return fail(KVPUB_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s",
+                        cudaGetErrorString(e));
+        p = static_cast<uint8_t *>(addr);
+        g_static_workspace_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return KVPUB_OK;
+}
+
+}  // namespace
+}  // namespace kvpub
+
+extern "C" kvpub_status kvpub_gather_insert_noalloc(
+    const void *kv_latent, int64_t latent_stride, const void *k_rope, int64_t rope_stride,
+    const void *index_k, int64_t index_stride, const int64_t *slot_mapping, int64_t num_tokens,
+    void *const *main_caches, void *const *indexer_caches, int num_replicas, int64_t num_blocks,
+    int block_size, unsigned long long *invalid_count, kvpub_stream_t stream) {
+    Validated v;
+    kvpub_status st = validate(kv_latent, latent_stride, k_rope, rope_stride, index_k,
+                               index_stride, slot_mapping, num_tokens, main_caches,
+                               indexer_caches, num_replicas, num_blocks, block_size,
+                               invalid_count, &v);
+    if (st != KVPUB_OK) return st;
+    if (num_tokens > KVPUB_STATIC_GATHER_MAX_TOKENS)
+        return fail(KVPUB_ERR_WORKSPACE,
+                    "num_tokens %lld exceeds the static workspace limit of %d tokens",
+                    (long long)num_tokens, KVPUB_STATIC_GATHER_MAX_TOKENS);
+    if (num_tokens == 0) return ok();
+    uint8_t *ws = nullptr;
+    if ((st = static_gather_workspace(&ws)) != KVPUB_OK) return st;
+    int grid = 0;
+    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    // Nothing in the array has to start at zero: the gather writes every
+    // row that the inserts then read, all in stream order.
+    (void)cudaGetLastError();
+    gather_rows_kernel<<<grid, kThreads, 0, s>>>(v.args, ws);
+    if ((st = launched("gather_rows(static)")) != KVPUB_OK) return st;
+    StoreArgs ins = v.args;
+    const uint16_t *w16 = reinterpret_cast<const uint16_t *>(ws);
+    ins.latent = w16;
+    ins.rope = w16 + KVPUB_LATENT_DIM;
+    ins.index_k = w16 + KVPUB_LATENT_DIM + KVPUB_ROPE_DIM;
+    ins.latent_stride = ins.rope_stride = ins.index_stride = KVPUB_GATHER_ROW_BYTES / 2;
+    for (int r = 0; r < v.num_replicas; ++r) {
+        ins.rep = Replicas{};
+        ins.rep.main[0] = v.args.rep.main[r];
+        ins.rep.indexer[0] = v.args.rep.indexer[r];
+        ins.invalid_count = (r == 0) ? v.args.invalid_count : nullptr;
+        store_mla_fp8_kernel<1><<<grid, kThreads, 0, s>>>(ins);
+        if ((st = launched("insert_rows(static)")) != KVPUB_OK) return st;
+    }
+    return ok();
+}

@@ -31,6 +31,7 @@ INDEXER_BLOCK_BYTES = BLOCK_SIZE * 132
 GATHER_ROW_BYTES = 1408
 MAX_REPLICAS = 8
 MAX_POLLS = 1 << 24
+STATIC_GATHER_MAX_TOKENS = 4096
 
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "ALIGNMENT", 3: "TOO_MANY_REPLICAS", 4: "CUDA",
           5: "WORKSPACE"}
@@ -57,6 +58,7 @@ SIGNATURES = {
     "kvpub_store_mla_fp8_publish": (_STORE_ARGS + [_vp, _vp, _vp], ctypes.c_int),
     "kvpub_gather_workspace_bytes": ([_i64], ctypes.c_size_t),
     "kvpub_gather_insert": (_STORE_ARGS + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "kvpub_gather_insert_noalloc": (_STORE_ARGS + [_vp], ctypes.c_int),
     "kvpub_epoch_advance": ([_vp, _vp], ctypes.c_int),
     "kvpub_epoch_wait": ([_vp, ctypes.c_uint64, ctypes.c_uint64, _vp, _vp], ctypes.c_int),
     "kvpub_last_error": ([], ctypes.c_char_p),
@@ -187,6 +189,17 @@ def gather_insert(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer
     nbytes = workspace.numel() * workspace.element_size()
     check(lib().kvpub_gather_insert(*args, workspace.data_ptr(), nbytes,
                                     _stream_handle(stream)))
+
+
+def gather_insert_noalloc(kv_latent, k_rope, index_k, slot_mapping, main_caches,
+                          indexer_caches, num_blocks=None, invalid_count=None,
+                          stream=None) -> None:
+    """gather_insert with the library's fixed workspace, for callers that may
+    not allocate device memory (at most STATIC_GATHER_MAX_TOKENS tokens;
+    calls that overlap on the GPU race on the shared workspace)."""
+    args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                       num_blocks, invalid_count)
+    check(lib().kvpub_gather_insert_noalloc(*args, _stream_handle(stream)))
 
 
 def _counter(t, dtypes, name):

@@ -115,6 +115,14 @@ def test_gather_rejects_small_or_missing_workspace(lib):
     assert lib.kvpub_gather_insert(*store_args(), A + 8, 10 ** 9, None) == 2
 
 
+def test_noalloc_rejects_bad_arguments_and_oversized_batches(lib):
+    for name, over, status in BAD:
+        assert lib.kvpub_gather_insert_noalloc(*store_args(**over), None) == status, name
+    limit = kvpub.STATIC_GATHER_MAX_TOKENS
+    assert lib.kvpub_gather_insert_noalloc(*store_args(T=limit + 1), None) == 5
+    assert "static workspace limit" in kvpub.last_error()
+
+
 def test_publish_rejects_bad_counters(lib):
     # invalid R keeps this call away from the GPU whatever the counters are
     assert lib.kvpub_store_mla_fp8_publish(*store_args(R=0), None, A, None) == 1
