@@ -235,32 +235,50 @@ class Step:
         x = self.rows[layer]
         return x[:, :512], x[:, 512:576], x[:, 576:704]
 
-    def launch_layers(self, events=None):
+    def launch_layers(self, with_epoch: bool = True):
         for layer in range(self.spec.layers):
-            lat, rope, idx = self.views(layer)
-            if events is not None:
-                events[2 * layer].record()
-            kvpub.store_mla_fp8(lat, rope, idx, self.slots[layer], self.main[layer],
-                                self.idx[layer], self.spec.num_blocks,
-                                invalid_count=self.invalid)
-            if events is not None:
-                events[2 * layer + 1].record()
+            self.launch_layer(layer, with_epoch)
+
+    def launch_layer(self, layer: int, with_epoch: bool = True):
+        lat, rope, idx = self.views(layer)
+        kvpub.store_mla_fp8(lat, rope, idx, self.slots[layer], self.main[layer],
+                            self.idx[layer], self.spec.num_blocks, invalid_count=self.invalid)
+        if with_epoch:
             kvpub.epoch_advance(self.epoch)
 
-    def capture(self, timed_events: bool):
-        events = None
-        if timed_events:
-            try:
-                events = [torch.cuda.Event(enable_timing=True, external=True)
-                          for _ in range(2 * self.spec.layers)]
-            except TypeError:
-                events = None
-        self.launch_layers()                     # load kernels before capture
+    def capture(self, with_epoch: bool = True):
+        """One graph of all layers: store (+ epoch advance) per layer."""
+        self.launch_layers(with_epoch=False)    # load the kernels before capture
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.launch_layers(events)
-        return g, events
+            self.launch_layers(with_epoch)
+        return g
+
+    def capture_end_to_end(self):
+        """One graph of a whole step from host memory: the slot maps and each
+        layer's pinned host rows are copied on a side stream, layer by layer,
+        while the stores of the layers already copied run; the epoch is read
+        back into pinned host memory at the end."""
+        L = self.spec.layers
+        self.host_epoch = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+        copy_stream = torch.cuda.Stream()
+        ready = [torch.cuda.Event() for _ in range(L)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            main = torch.cuda.current_stream()
+            copy_stream.wait_stream(main)
+            with torch.cuda.stream(copy_stream):
+                self.slots.copy_(self.host_slots, non_blocking=True)
+                for layer in range(L):
+                    self.rows[layer].copy_(self.host_rows[layer], non_blocking=True)
+                    ready[layer].record(copy_stream)
+            for layer in range(L):
+                main.wait_event(ready[layer])
+                self.launch_layer(layer)
+            self.host_epoch.copy_(self.epoch, non_blocking=True)
+            main.wait_stream(copy_stream)
+        return g
 
 
 def time_graph(g, steps, warmup):
@@ -297,33 +315,19 @@ def max_over_ranks(x: float) -> float:
 
 
 def e2e_measure(step: Step, steps: int, warmup: int):
-    """Through the public API with host inputs: every step copies the 61
-    layers' pinned host rows and the slot_mapping to the device, runs the
-    61 stores and epoch advances, and reads the epoch back to the host."""
-    dev = step.dev
-    host_epoch = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    """Through the public API with host inputs: every step copies all layers'
+    pinned host rows and slot maps to the device, runs every store and epoch
+    advance, and reads the epoch back to pinned host memory."""
     h2d = step.host_rows.numel() * 2 + step.host_slots.numel() * 8
     d2h = 8
-
-    def run_once():
-        step.rows.copy_(step.host_rows, non_blocking=True)
-        step.slots.copy_(step.host_slots, non_blocking=True)
-        step.launch_layers()
-        host_epoch.copy_(step.epoch, non_blocking=True)
-
-    for _ in range(warmup):
-        run_once()
-    torch.cuda.synchronize()
-    barrier()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        run_once()
-    end.record()
-    torch.cuda.synchronize()
-    barrier()
-    return start.elapsed_time(end), h2d, d2h, int(host_epoch.item())
+    g = step.capture_end_to_end()
+    before = int(step.epoch.item())
+    ms, _, _ = time_graph(g, steps, warmup)
+    after = int(step.host_epoch.item())
+    if after != before + step.spec.layers * (warmup + steps):
+        raise RuntimeError(f"end-to-end epoch read back {after}, expected "
+                           f"{before + step.spec.layers * (warmup + steps)}")
+    return ms, h2d, d2h
 
 
 def cpu_baseline(budget_s: float):
@@ -357,12 +361,14 @@ def run_ours(args):
     spec = SPECS[args.workload]()
     step = Step(dev, spec)
     L, Rr = spec.layers, spec.replicas
-    g, events = step.capture(timed_events=True)
+    g = step.capture(with_epoch=True)
+    g_store = step.capture(with_epoch=False)
     with ClockSampler(local) as clocks:
         total_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
+        store_ms, _, _ = time_graph(g_store, args.steps, args.warmup)
     total_ms = max_over_ranks(total_ms)
     ms_per_step = total_ms / args.steps
-    expected_epoch = L * (1 + args.warmup + args.steps)
+    expected_epoch = L * (args.warmup + args.steps)
     epoch = int(step.epoch.item())
     if epoch != expected_epoch:
         raise RuntimeError(f"epoch {epoch} != {expected_epoch}: launches were lost")
@@ -372,13 +378,9 @@ def run_ours(args):
     launch_bytes = [store_bytes(step.num_tokens, v, Rr) for v in step.valid]
     per_launch = sum(launch_bytes) / L
     peak, peak_kind = measured_peak()
-    if events is not None:
-        durs = [events[2 * k].elapsed_time(events[2 * k + 1]) for k in range(L)]
-        kernel_ms = sum(durs) / len(durs)
-        timing = f"CUDA events around each of the {L} store launches in the last timed replay"
-    else:
-        kernel_ms = ms_per_step / L
-        timing = f"step time / {L} (this torch cannot record events inside a graph)"
+    kernel_ms = store_ms / (args.steps * L)
+    timing = (f"CUDA events around {args.steps} replays of a graph of the same {L} store "
+              f"launches (no epoch kernels) / {args.steps * L} launches, gaps included")
     achieved = per_launch / (kernel_ms / 1e3) / 1e9
     traffic = profiled_traffic() if spec.name == WORKLOAD else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -391,7 +393,7 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 50))
-        e2e_ms, h2d, d2h, _ = e2e_measure(step, e2e_steps, max(1, min(args.warmup, 3)))
+        e2e_ms, h2d, d2h = e2e_measure(step, e2e_steps, max(1, min(args.warmup, 3)))
         e2e_ms = max_over_ranks(e2e_ms)
         e2e = {"value": world * rows_x_r / (e2e_ms / e2e_steps / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -57,34 +57,56 @@ __device__ __forceinline__ uint2 ld_stream8(const void *p) {
     return v;
 }
 
+// Stores are cache-streaming (evict-first): nothing written here is read
+// again by this launch.
 __device__ __forceinline__ void st16(void *p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Plain store, for the gather workspace that the insert launches read back.
+__device__ __forceinline__ void st16_keep(void *p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
 __device__ __forceinline__ void st4(void *p, uint32_t v) {
-    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+    asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
-// One token row, quantised and stored to every replica.  All lanes of the
-// warp call this together (s is warp-uniform).
-template <int R>
-__device__ __forceinline__ void publish_row(const StoreArgs &a, int64_t t, int64_t s,
-                                            int lane) {
-    const uint8_t *lat = reinterpret_cast<const uint8_t *>(a.latent + t * a.latent_stride);
-    const uint4 x0 = ld_stream16(lat + 32 * lane);
-    const uint4 x1 = ld_stream16(lat + 32 * lane + 16);
-    const uint2 xi = ld_stream8(reinterpret_cast<const uint8_t *>(a.index_k + t * a.index_stride) +
-                                8 * lane);
-    uint4 tail = make_uint4(0u, 0u, 0u, 0u);
-    if (lane >= 1 && lane <= 8)
-        tail = ld_stream16(reinterpret_cast<const uint8_t *>(a.rope + t * a.rope_stride) +
-                           16 * (lane - 1));
+// One token row's inputs as this lane holds them.
+struct RowRegs {
+    uint4 x0, x1;   // latent elements [16 l, 16 l + 16)
+    uint2 xi;       // Indexer-K elements [4 l, 4 l + 4)
+    uint4 tail;     // lanes 1..8: rope chunk l - 1
+};
 
+__device__ __forceinline__ void load_row(const StoreArgs &a, int64_t t, int lane, RowRegs &v) {
+    const uint8_t *lat = reinterpret_cast<const uint8_t *>(a.latent + t * a.latent_stride);
+    v.x0 = ld_stream16(lat + 32 * lane);
+    v.x1 = ld_stream16(lat + 32 * lane + 16);
+    v.xi = ld_stream8(reinterpret_cast<const uint8_t *>(a.index_k + t * a.index_stride) +
+                      8 * lane);
+    v.tail = make_uint4(0u, 0u, 0u, 0u);
+    if (lane >= 1 && lane <= 8)
+        v.tail = ld_stream16(reinterpret_cast<const uint8_t *>(a.rope + t * a.rope_stride) +
+                             16 * (lane - 1));
+}
+
+__device__ __forceinline__ bool slot_written(int64_t s, int64_t num_slots) {
+    return s >= 0 && s < num_slots;
+}
+
+// Quantise one row held in registers and store it to every replica.  All
+// lanes of the warp call this together (s is warp-uniform).
+template <int R>
+__device__ __forceinline__ void publish_row(const StoreArgs &a, const RowRegs &v, int64_t s,
+                                            int lane) {
     // amax: latent tile (8 lanes) in the low half, Indexer-K (32 lanes) high.
-    uint32_t m_lat = absmax_bf16x2(absmax_bf16x2(x0.x, x0.y), absmax_bf16x2(x0.z, x0.w));
-    m_lat = __vmaxu2(m_lat, absmax_bf16x2(absmax_bf16x2(x1.x, x1.y), absmax_bf16x2(x1.z, x1.w)));
-    const uint32_t m_idx = halves_max(absmax_bf16x2(xi.x, xi.y));
+    uint32_t m_lat = absmax_bf16x2(absmax_bf16x2(v.x0.x, v.x0.y), absmax_bf16x2(v.x0.z, v.x0.w));
+    m_lat = __vmaxu2(m_lat, absmax_bf16x2(absmax_bf16x2(v.x1.x, v.x1.y),
+                                          absmax_bf16x2(v.x1.z, v.x1.w)));
+    const uint32_t m_idx = halves_max(absmax_bf16x2(v.xi.x, v.xi.y));
     uint32_t packed = halves_max(m_lat) | (m_idx << 16);
     packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 1));
     packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 2));
@@ -94,16 +116,18 @@ __device__ __forceinline__ void publish_row(const StoreArgs &a, int64_t t, int64
     packed = __vmaxu2(packed, __shfl_xor_sync(kFullMask, packed, 16));
     const float s_idx = tile_scale(packed >> 16);
 
-    const uint2 q0 = quant_bf16x8(x0, s_lat);
-    const uint2 q1 = quant_bf16x8(x1, s_lat);
-    const uint4 q_lat = make_uint4(q0.x, q0.y, q1.x, q1.y);
-    const uint32_t q_idx = quant_bf16x2(xi.x, s_idx) | (quant_bf16x2(xi.y, s_idx) << 16);
+    const TileDivisor d_lat = tile_divisor(s_lat);
+    const TileDivisor d_idx = tile_divisor(s_idx);
+    const uint4 q_lat = make_uint4(quant4(v.x0.x, v.x0.y, d_lat), quant4(v.x0.z, v.x0.w, d_lat),
+                                   quant4(v.x1.x, v.x1.y, d_lat), quant4(v.x1.z, v.x1.w, d_lat));
+    const uint32_t q_idx = quant4(v.xi.x, v.xi.y, d_idx);
 
     // lane 0 carries the 4 tile scales (row bytes 512..527); lanes 1..8
     // carry the rope (bytes 528..655).
     const float s1 = __shfl_sync(kFullMask, s_lat, 8);
     const float s2 = __shfl_sync(kFullMask, s_lat, 16);
     const float s3 = __shfl_sync(kFullMask, s_lat, 24);
+    uint4 tail = v.tail;
     if (lane == 0)
         tail = make_uint4(__float_as_uint(s_lat), __float_as_uint(s1), __float_as_uint(s2),
                           __float_as_uint(s3));
@@ -124,20 +148,35 @@ __device__ __forceinline__ void publish_row(const StoreArgs &a, int64_t t, int64
     }
 }
 
-// Grid-stride over token rows, one warp per row.
+// Grid-stride over token rows, one warp per row.  The next row's slot and
+// inputs are loaded before the current row is quantised, so each warp keeps
+// two rows of loads in flight.
 template <int R>
 __device__ __forceinline__ void publish_rows(const StoreArgs &a) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t t = warp; t < a.num_tokens; t += num_warps) {
-        const int64_t s = a.slot_mapping[t];
-        if (s < 0 || s >= a.num_slots) {
-            if (s != -1 && lane == 0 && a.invalid_count != nullptr)
-                atomicAdd(a.invalid_count, 1ull);
-            continue;
+    int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (t >= a.num_tokens) return;
+    int64_t s = a.slot_mapping[t];
+    RowRegs cur;
+    if (slot_written(s, a.num_slots)) load_row(a, t, lane, cur);
+    while (true) {
+        const int64_t t_next = t + num_warps;
+        int64_t s_next = -1;
+        RowRegs nxt;
+        if (t_next < a.num_tokens) {
+            s_next = a.slot_mapping[t_next];
+            if (slot_written(s_next, a.num_slots)) load_row(a, t_next, lane, nxt);
         }
-        publish_row<R>(a, t, s, lane);
+        if (slot_written(s, a.num_slots)) {
+            publish_row<R>(a, cur, s, lane);
+        } else if (s != -1 && lane == 0 && a.invalid_count != nullptr) {
+            atomicAdd(a.invalid_count, 1ull);
+        }
+        if (t_next >= a.num_tokens) break;
+        t = t_next;
+        s = s_next;
+        cur = nxt;
     }
 }
 
@@ -188,7 +227,7 @@ gather_rows_kernel(const StoreArgs a, uint8_t *workspace) {
             const uint8_t *src = c < 64 ? lat + 16 * c
                                 : c < 72 ? rope + 16 * (c - 64)
                                          : idx + 16 * (c - 72);
-            st16(w + 16 * c, ld_stream16(src));
+            st16_keep(w + 16 * c, ld_stream16(src));
         }
     }
 }
@@ -311,40 +350,51 @@ kvpub_status validate(const void *kv_latent, int64_t latent_stride, const void *
     return KVPUB_OK;
 }
 
-// Resident blocks per SM for each kernel, times the SM count, per device.
+// SM count and, per kernel, resident blocks per SM; both cached per device.
 constexpr int kMaxDevices = 64;
 
-struct DeviceInfo {
-    std::atomic<int> sm_count{0};
-};
-DeviceInfo g_devices[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
 
-kvpub_status sm_count(int *out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+kvpub_status current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return fail(KVPUB_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return fail(KVPUB_ERR_CUDA, "device %d out of range", dev);
-    int n = g_devices[dev].sm_count.load(std::memory_order_relaxed);
+    if (*dev < 0 || *dev >= kMaxDevices)
+        return fail(KVPUB_ERR_CUDA, "device %d out of range", *dev);
+    return KVPUB_OK;
+}
+
+kvpub_status sm_count(int dev, int *out) {
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
     if (n == 0) {
-        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return fail(KVPUB_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
-        g_devices[dev].sm_count.store(n, std::memory_order_relaxed);
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
     }
     *out = n;
     return KVPUB_OK;
 }
 
-// Blocks for a grid-stride pass over num_tokens rows: enough to give every
-// row a warp, capped at kBlocksPerSm resident waves.
-constexpr int kBlocksPerSm = 8;
-
-kvpub_status grid_for(int64_t num_tokens, int *grid) {
-    int sms = 0;
-    kvpub_status st = sm_count(&sms);
+// A grid-stride pass over num_tokens rows (one warp per row): one block per
+// kWarpsPerBlock rows, capped at the blocks that fit on the GPU at once, so
+// every launch is a single wave.
+template <typename Kernel>
+kvpub_status one_wave_grid(Kernel kernel, std::atomic<int> *resident, int64_t num_tokens,
+                           int *grid) {
+    int dev = 0, sms = 0;
+    kvpub_status st = current_device(&dev);
     if (st != KVPUB_OK) return st;
+    if ((st = sm_count(dev, &sms)) != KVPUB_OK) return st;
+    int per_sm = resident[dev].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+        if (e != cudaSuccess)
+            return fail(KVPUB_ERR_CUDA, "occupancy query: %s", cudaGetErrorString(e));
+        if (per_sm < 1) per_sm = 1;
+        resident[dev].store(per_sm, std::memory_order_relaxed);
+    }
     int64_t want = (num_tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    int64_t cap = static_cast<int64_t>(sms) * kBlocksPerSm;
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
     if (want > cap) want = cap;
     if (want < 1) want = 1;
     *grid = static_cast<int>(want);
@@ -358,33 +408,78 @@ kvpub_status launched(const char *what) {
 }
 
 template <template <int> class Launch, typename... Args>
-void dispatch_replicas(int r, Args &&...args) {
+kvpub_status dispatch_replicas(int r, Args &&...args) {
     switch (r) {
-        case 1: Launch<1>::go(args...); break;
-        case 2: Launch<2>::go(args...); break;
-        case 3: Launch<3>::go(args...); break;
-        case 4: Launch<4>::go(args...); break;
-        case 5: Launch<5>::go(args...); break;
-        case 6: Launch<6>::go(args...); break;
-        case 7: Launch<7>::go(args...); break;
-        default: Launch<8>::go(args...); break;
+        case 1: return Launch<1>::go(args...);
+        case 2: return Launch<2>::go(args...);
+        case 3: return Launch<3>::go(args...);
+        case 4: return Launch<4>::go(args...);
+        case 5: return Launch<5>::go(args...);
+        case 6: return Launch<6>::go(args...);
+        case 7: return Launch<7>::go(args...);
+        default: return Launch<8>::go(args...);
     }
 }
 
 template <int R>
 struct LaunchStore {
-    static void go(int grid, cudaStream_t stream, const StoreArgs &a) {
+    static std::atomic<int> resident[kMaxDevices];
+    static kvpub_status go(cudaStream_t stream, const StoreArgs &a) {
+        int grid = 0;
+        kvpub_status st = one_wave_grid(store_mla_fp8_kernel<R>, resident, a.num_tokens, &grid);
+        if (st != KVPUB_OK) return st;
+        (void)cudaGetLastError();
         store_mla_fp8_kernel<R><<<grid, kThreads, 0, stream>>>(a);
+        return launched("store_mla_fp8");
     }
 };
+template <int R>
+std::atomic<int> LaunchStore<R>::resident[kMaxDevices];
 
 template <int R>
 struct LaunchPublish {
-    static void go(int grid, cudaStream_t stream, const StoreArgs &a, unsigned long long *epoch,
-                   unsigned int *done) {
+    static std::atomic<int> resident[kMaxDevices];
+    static kvpub_status go(cudaStream_t stream, const StoreArgs &a, unsigned long long *epoch,
+                           unsigned int *done) {
+        int grid = 0;
+        kvpub_status st =
+            one_wave_grid(store_mla_fp8_publish_kernel<R>, resident, a.num_tokens, &grid);
+        if (st != KVPUB_OK) return st;
+        (void)cudaGetLastError();
         store_mla_fp8_publish_kernel<R><<<grid, kThreads, 0, stream>>>(a, epoch, done);
+        return launched("store_mla_fp8_publish");
     }
 };
+template <int R>
+std::atomic<int> LaunchPublish<R>::resident[kMaxDevices];
+
+std::atomic<int> g_gather_resident[kMaxDevices];
+
+// Gather every row into the workspace, then one insert launch per replica
+// that quantises the gathered rows (the insert is the store kernel with one
+// replica, reading the workspace rows).
+kvpub_status gather_then_insert(const Validated &v, uint8_t *ws, cudaStream_t s) {
+    int grid = 0;
+    kvpub_status st = one_wave_grid(gather_rows_kernel, g_gather_resident, v.args.num_tokens, &grid);
+    if (st != KVPUB_OK) return st;
+    (void)cudaGetLastError();
+    gather_rows_kernel<<<grid, kThreads, 0, s>>>(v.args, ws);
+    if ((st = launched("gather_rows")) != KVPUB_OK) return st;
+    StoreArgs ins = v.args;
+    const uint16_t *w16 = reinterpret_cast<const uint16_t *>(ws);
+    ins.latent = w16;
+    ins.rope = w16 + KVPUB_LATENT_DIM;
+    ins.index_k = w16 + KVPUB_LATENT_DIM + KVPUB_ROPE_DIM;
+    ins.latent_stride = ins.rope_stride = ins.index_stride = KVPUB_GATHER_ROW_BYTES / 2;
+    for (int r = 0; r < v.num_replicas; ++r) {
+        ins.rep = Replicas{};
+        ins.rep.main[0] = v.args.rep.main[r];
+        ins.rep.indexer[0] = v.args.rep.indexer[r];
+        ins.invalid_count = (r == 0) ? v.args.invalid_count : nullptr;
+        if ((st = LaunchStore<1>::go(s, ins)) != KVPUB_OK) return st;
+    }
+    return ok();
+}
 
 }  // namespace
 }  // namespace kvpub
@@ -403,11 +498,7 @@ extern "C" kvpub_status kvpub_store_mla_fp8(
                                invalid_count, &v);
     if (st != KVPUB_OK) return st;
     if (num_tokens == 0) return ok();
-    int grid = 0;
-    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
-    (void)cudaGetLastError();
-    dispatch_replicas<LaunchStore>(v.num_replicas, grid, (cudaStream_t)stream, v.args);
-    return launched("store_mla_fp8");
+    return dispatch_replicas<LaunchStore>(v.num_replicas, (cudaStream_t)stream, v.args);
 }
 
 extern "C" kvpub_status kvpub_store_mla_fp8_publish(
@@ -426,12 +517,8 @@ extern "C" kvpub_status kvpub_store_mla_fp8_publish(
         return fail(KVPUB_ERR_INVALID_ARG, "epoch or done_count is NULL");
     if (!aligned(epoch, 8) || !aligned(done_count, 4))
         return fail(KVPUB_ERR_ALIGNMENT, "epoch or done_count is misaligned");
-    int grid = 0;
-    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
-    (void)cudaGetLastError();
-    dispatch_replicas<LaunchPublish>(v.num_replicas, grid, (cudaStream_t)stream, v.args, epoch,
-                                     done_count);
-    return launched("store_mla_fp8_publish");
+    return dispatch_replicas<LaunchPublish>(v.num_replicas, (cudaStream_t)stream, v.args, epoch,
+                                            done_count);
 }
 
 extern "C" size_t kvpub_gather_workspace_bytes(int64_t num_tokens) {
@@ -458,29 +545,7 @@ extern "C" kvpub_status kvpub_gather_insert(
     if (workspace_bytes < kvpub_gather_workspace_bytes(num_tokens))
         return fail(KVPUB_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", workspace_bytes,
                     kvpub_gather_workspace_bytes(num_tokens));
-    int grid = 0;
-    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    (void)cudaGetLastError();
-    gather_rows_kernel<<<grid, kThreads, 0, s>>>(v.args, ws);
-    if ((st = launched("gather_rows")) != KVPUB_OK) return st;
-    // Insert: each replica quantises the gathered rows on its own.
-    StoreArgs ins = v.args;
-    const uint16_t *w16 = reinterpret_cast<const uint16_t *>(ws);
-    ins.latent = w16;
-    ins.rope = w16 + KVPUB_LATENT_DIM;
-    ins.index_k = w16 + KVPUB_LATENT_DIM + KVPUB_ROPE_DIM;
-    ins.latent_stride = ins.rope_stride = ins.index_stride = KVPUB_GATHER_ROW_BYTES / 2;
-    for (int r = 0; r < v.num_replicas; ++r) {
-        ins.rep = Replicas{};
-        ins.rep.main[0] = v.args.rep.main[r];
-        ins.rep.indexer[0] = v.args.rep.indexer[r];
-        ins.invalid_count = (r == 0) ? v.args.invalid_count : nullptr;
-        store_mla_fp8_kernel<1><<<grid, kThreads, 0, s>>>(ins);
-        if ((st = launched("insert_rows")) != KVPUB_OK) return st;
-    }
-    return ok();
+    return gather_then_insert(v, static_cast<uint8_t *>(workspace), (cudaStream_t)stream);
 }
 
 extern "C" kvpub_status kvpub_epoch_advance(unsigned long long *epoch, kvpub_stream_t stream) {
@@ -529,13 +594,12 @@ std::atomic<uint8_t *> g_static_workspace_addr[kMaxDevices];
 
 kvpub_status static_gather_workspace(uint8_t **out) {
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(KVPUB_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return fail(KVPUB_ERR_CUDA, "device %d out of range", dev);
+    kvpub_status st = current_device(&dev);
+    if (st != KVPUB_OK) return st;
     uint8_t *p = g_static_workspace_addr[dev].load(std::memory_order_acquire);
     if (p == nullptr) {
         void *addr = nullptr;
-        e = cudaGetSymbolAddress(&addr, g_static_gather_workspace);
+        cudaError_t e = cudaGetSymbolAddress(&addr, g_static_gather_workspace);
         if (e != cudaSuccess || addr == nullptr)
             return fail(KVPUB_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s",
                         cudaGetErrorString(e));
@@ -567,27 +631,7 @@ extern "C" kvpub_status kvpub_gather_insert_noalloc(
     if (num_tokens == 0) return ok();
     uint8_t *ws = nullptr;
     if ((st = static_gather_workspace(&ws)) != KVPUB_OK) return st;
-    int grid = 0;
-    if ((st = grid_for(num_tokens, &grid)) != KVPUB_OK) return st;
-    cudaStream_t s = (cudaStream_t)stream;
     // Nothing in the array has to start at zero: the gather writes every
     // row that the inserts then read, all in stream order.
-    (void)cudaGetLastError();
-    gather_rows_kernel<<<grid, kThreads, 0, s>>>(v.args, ws);
-    if ((st = launched("gather_rows(static)")) != KVPUB_OK) return st;
-    StoreArgs ins = v.args;
-    const uint16_t *w16 = reinterpret_cast<const uint16_t *>(ws);
-    ins.latent = w16;
-    ins.rope = w16 + KVPUB_LATENT_DIM;
-    ins.index_k = w16 + KVPUB_LATENT_DIM + KVPUB_ROPE_DIM;
-    ins.latent_stride = ins.rope_stride = ins.index_stride = KVPUB_GATHER_ROW_BYTES / 2;
-    for (int r = 0; r < v.num_replicas; ++r) {
-        ins.rep = Replicas{};
-        ins.rep.main[0] = v.args.rep.main[r];
-        ins.rep.indexer[0] = v.args.rep.indexer[r];
-        ins.invalid_count = (r == 0) ? v.args.invalid_count : nullptr;
-        store_mla_fp8_kernel<1><<<grid, kThreads, 0, s>>>(ins);
-        if ((st = launched("insert_rows(static)")) != KVPUB_OK) return st;
-    }
-    return ok();
+    return gather_then_insert(v, ws, (cudaStream_t)stream);
 }

@@ -11,6 +11,18 @@
 // amax = max |x|, scale = max(amax, 1e-4f) / 448 (one IEEE fp32 division),
 // code = E4M3(x / scale) with round-to-nearest-even and saturation; a NaN in
 // the tile gives the scale 0x7FFFFFFF and codes 0x7F.
+//
+// The quotient x / scale must be the correctly rounded fp32 quotient.  It is
+// computed with Markstein's correction (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with y = RN(1/scale) from one IEEE reciprocal per
+// tile, q0 = RN(x * y), r = x - scale * q0 (exact in one fma) and
+// q = RN(q0 + r * y) (one fma).  Per element that is one multiply and two
+// fmas, issued two elements at a time as packed f32x2 operations, then the
+// input's sign bit is ORed into each code (see quant4_markstein).  A tile
+// whose scale is not finite (an Inf or NaN in the tile) takes IEEE division.
+// Over every (x, amax) pair the kernel can meet, the codes this produces
+// equal those of IEEE division; a GPU test sweeps all of them.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -40,20 +52,81 @@ __device__ __forceinline__ float tile_scale(uint32_t amax_bits16) {
     return s;
 }
 
-// Two bf16 (one 32-bit word) -> two E4M3 codes (low byte = low element).
-__device__ __forceinline__ uint32_t quant_bf16x2(uint32_t w, float scale) {
-    const float lo = __uint_as_float(w << 16);
-    const float hi = __uint_as_float(w & 0xffff0000u);
-    const float2 q = make_float2(__fdiv_rn(lo, scale), __fdiv_rn(hi, scale));
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3));
+// Everything a lane needs to divide by one tile's scale.
+struct TileDivisor {
+    float scale;
+    unsigned long long y2;        // {RN(1/scale), RN(1/scale)}
+    unsigned long long neg_s2;    // {-scale, -scale}
+    bool ieee;                    // scale is Inf or NaN: use IEEE division
+};
+
+__device__ __forceinline__ TileDivisor tile_divisor(float scale) {
+    TileDivisor d;
+    d.scale = scale;
+    d.ieee = !(fabsf(scale) <= 3.402823466e38f);
+    const float y = __frcp_rn(scale);
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d.y2) : "f"(y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d.neg_s2) : "f"(-scale));
+    return d;
 }
 
-// Four bf16 words (8 values) -> 8 codes packed in two 32-bit words.
-__device__ __forceinline__ uint2 quant_bf16x8(uint4 v, float scale) {
-    uint2 out;
-    out.x = quant_bf16x2(v.x, scale) | (quant_bf16x2(v.y, scale) << 16);
-    out.y = quant_bf16x2(v.z, scale) | (quant_bf16x2(v.w, scale) << 16);
+// Two bf16 words (4 values) -> 4 E4M3 codes, low byte = first value, using
+// Markstein's correction on packed f32x2.  For x = -0 the residual
+// fma(-scale, q0, x) is (+0) + (-0) = +0 and the corrected quotient comes
+// out +0, so the sign of each input is ORed into its code afterwards: for
+// every finite x the correctly rounded quotient carries the sign of x, and
+// for x != -0 the code already has it.
+__device__ __forceinline__ uint32_t quant4_markstein(uint32_t w0, uint32_t w1,
+                                                     unsigned long long y2,
+                                                     unsigned long long neg_s2) {
+    uint32_t out;
+    asm("{\n\t"
+        ".reg .b32 l0, h0, l1, h1;\n\t"
+        ".reg .b64 x0, x1, a0, a1, r0, r1;\n\t"
+        ".reg .f32 p0, p1, p2, p3;\n\t"
+        ".reg .b16 c0, c1;\n\t"
+        ".reg .b32 codes, signs;\n\t"
+        "shl.b32 l0, %1, 16;\n\t"
+        "and.b32 h0, %1, 0xffff0000;\n\t"
+        "shl.b32 l1, %2, 16;\n\t"
+        "and.b32 h1, %2, 0xffff0000;\n\t"
+        "mov.b64 x0, {l0, h0};\n\t"
+        "mov.b64 x1, {l1, h1};\n\t"
+        "mul.rn.f32x2 a0, x0, %3;\n\t"
+        "mul.rn.f32x2 a1, x1, %3;\n\t"
+        "fma.rn.f32x2 r0, %4, a0, x0;\n\t"
+        "fma.rn.f32x2 r1, %4, a1, x1;\n\t"
+        "fma.rn.f32x2 a0, r0, %3, a0;\n\t"
+        "fma.rn.f32x2 a1, r1, %3, a1;\n\t"
+        "mov.b64 {p0, p1}, a0;\n\t"
+        "mov.b64 {p2, p3}, a1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 c0, p1, p0;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 c1, p3, p2;\n\t"
+        "mov.b32 codes, {c0, c1};\n\t"
+        // sign bits of the four inputs (bits 15 and 31 of each word) into
+        // bit 7 of their codes
+        "prmt.b32 signs, %1, %2, 0x7531;\n\t"
+        "lop3.b32 %0, codes, signs, 0x80808080, 0xF8;\n\t"
+        "}"
+        : "=r"(out)
+        : "r"(w0), "r"(w1), "l"(y2), "l"(neg_s2));
     return out;
+}
+
+// The same four codes through IEEE division (non-finite scales only).
+__device__ __forceinline__ uint32_t quant4_ieee(uint32_t w0, uint32_t w1, float scale) {
+    const float2 a = make_float2(__fdiv_rn(__uint_as_float(w0 << 16), scale),
+                                 __fdiv_rn(__uint_as_float(w0 & 0xffff0000u), scale));
+    const float2 b = make_float2(__fdiv_rn(__uint_as_float(w1 << 16), scale),
+                                 __fdiv_rn(__uint_as_float(w1 & 0xffff0000u), scale));
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint32_t quant4(uint32_t w0, uint32_t w1, const TileDivisor &d) {
+    if (d.ieee) return quant4_ieee(w0, w1, d.scale);
+    return quant4_markstein(w0, w1, d.y2, d.neg_s2);
 }
 
 }  // namespace kvpub

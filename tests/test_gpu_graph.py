@@ -111,3 +111,41 @@ def test_separate_epoch_lanes_in_one_graph(dev):
         g.replay()
         torch.cuda.synchronize()
         assert lanes.tolist() == [7 * k, 4 * k]
+
+
+def test_bench_step_matches_oracle(dev):
+    """The benchmark's own launch configuration: packed [T, 704] rows passed
+    as strided views, one graph of 61 x (store + epoch advance), and the
+    end-to-end graph that copies the inputs from pinned host memory."""
+    import bench
+
+    step = bench.Step(dev, bench.SPECS[bench.WORKLOAD]())
+    g = step.capture(with_epoch=True)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(step.epoch.item()) == LAYERS
+    slots = inputs.layer_slot_mapping()
+    for layer in (0, 31, 60):
+        w = inputs.prefill_layer(layer, slots)
+        want_main, want_idx, _, _ = oracle_caches(w)
+        for r in range(4):
+            assert np.array_equal(step.main[layer][r].cpu().numpy(), want_main[r])
+            assert np.array_equal(step.idx[layer][r].cpu().numpy(), want_idx[r])
+    # end to end: wipe the device rows and caches, then one replay must
+    # bring the rows back from host memory and rewrite the same bytes
+    step.rows.zero_()
+    for layer in (0, 60):
+        for c in step.main[layer] + step.idx[layer]:
+            c.fill_(inputs.GUARD_BYTE)
+    ge = step.capture_end_to_end()
+    ge.replay()
+    torch.cuda.synchronize()
+    assert int(step.host_epoch.item()) == 2 * LAYERS
+    for layer in (0, 60):
+        w = inputs.prefill_layer(layer, slots)
+        want_main, want_idx, _, _ = oracle_caches(w)
+        for r in range(4):
+            assert np.array_equal(step.main[layer][r].cpu().numpy(), want_main[r])
+            assert np.array_equal(step.idx[layer][r].cpu().numpy(), want_idx[r])
+    del step, g, ge
+    torch.cuda.empty_cache()
