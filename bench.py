@@ -197,6 +197,9 @@ SPECS = {
     "capacity_706624": lambda: Spec(
         "capacity_706624", 4, _copy_of(4), 4, 11041,
         "4 buffer copies of the 706,624-slot capacity batch per step"),
+    "capacity_706624_x1": lambda: Spec(
+        "capacity_706624_x1", 1, _copy_of(4), 4, 11041,
+        "one copy of the capacity batch (profiling case, ~2.3 GB)"),
     "stress_131072": lambda: Spec(
         "stress_131072", 1, _stress, 4, 8192,
         "one 131,072-row launch (profiling case)"),
