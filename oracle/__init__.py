@@ -43,6 +43,8 @@ MAIN_SLOT_BYTES = 656
 INDEXER_SLOT_BYTES = 132
 INDEXER_BLOCK_BYTES = BLOCK_SIZE * INDEXER_SLOT_BYTES
 ROW_BF16 = LATENT_DIM + ROPE_DIM + INDEXER_DIM
+MAIN_SLOT_BYTES_BF16 = 2 * (LATENT_DIM + ROPE_DIM)
+INDEXER_SLOT_BYTES_BF16 = 2 * INDEXER_DIM
 
 _lib = None
 _lock = threading.Lock()
@@ -83,6 +85,8 @@ def _load():
         lib.kvo_store_mla_fp8.restype = ctypes.c_int64
         lib.kvo_gather_insert.argtypes = common + [u16p, i64p]
         lib.kvo_gather_insert.restype = ctypes.c_int64
+        lib.kvo_store_mla_bf16.argtypes = common + [i64p]
+        lib.kvo_store_mla_bf16.restype = ctypes.c_int64
         _lib = lib
         return lib
 
@@ -194,6 +198,42 @@ def gather_insert(kv_latent, k_rope, index_k, slot_mapping, main_caches,
         _cache_ptrs(main_caches), _cache_ptrs(indexer_caches), len(main_caches),
         int(num_blocks), _ptr(ws, ctypes.c_uint16), ctypes.byref(inv))
     return int(n), int(inv.value)
+
+
+def store_mla_bf16(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                   num_blocks):
+    """Unquantised variant: the bf16 rows stored as they are into every
+    replica (Main slot 1152 B, Indexer slot 256 B).  Returns (rows written
+    per replica, invalid slot count)."""
+    lat, ls = _rows(kv_latent, LATENT_DIM)
+    rope, rs = _rows(k_rope, ROPE_DIM)
+    idx, ids = _rows(index_k, INDEXER_DIM)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T = slots.shape[0]
+    if not (lat.shape[0] >= T and rope.shape[0] >= T and idx.shape[0] >= T):
+        raise ValueError("fewer input rows than slot_mapping entries")
+    if len(main_caches) != len(indexer_caches) or not main_caches:
+        raise ValueError("need the same number (>= 1) of Main and Indexer caches")
+    for m, ix in zip(main_caches, indexer_caches):
+        if (m.nbytes < num_blocks * BLOCK_SIZE * MAIN_SLOT_BYTES_BF16
+                or ix.nbytes < num_blocks * BLOCK_SIZE * INDEXER_SLOT_BYTES_BF16):
+            raise ValueError("cache too small")
+    inv = ctypes.c_int64()
+    n = _load().kvo_store_mla_bf16(
+        _ptr(lat, ctypes.c_uint16), ls, _ptr(rope, ctypes.c_uint16), rs,
+        _ptr(idx, ctypes.c_uint16), ids, _ptr(slots, ctypes.c_int64), T,
+        _cache_ptrs(main_caches), _cache_ptrs(indexer_caches), len(main_caches),
+        int(num_blocks), ctypes.byref(inv))
+    return int(n), int(inv.value)
+
+
+def new_caches_bf16(num_replicas: int, num_blocks: int, guard: int = 0xA5):
+    """Fresh guard-filled host caches of the bf16 variant: (main, indexer)."""
+    main = [np.full(num_blocks * BLOCK_SIZE * MAIN_SLOT_BYTES_BF16, guard, np.uint8)
+            for _ in range(num_replicas)]
+    idx = [np.full(num_blocks * BLOCK_SIZE * INDEXER_SLOT_BYTES_BF16, guard, np.uint8)
+           for _ in range(num_replicas)]
+    return main, idx
 
 
 def new_caches(num_replicas: int, num_blocks: int, guard: int = 0xA5):

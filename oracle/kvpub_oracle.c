@@ -279,3 +279,45 @@ int64_t kvo_gather_insert(const uint16_t *kv_latent, int64_t latent_stride,
     if (invalid_out) *invalid_out = invalid;
     return written;
 }
+
+/*
+ * Unquantised (bf16) cache variant of direct publication: the same rows,
+ * slots and replicas, with the bytes stored as they arrive.  Covers the BF16
+ * main/indexer cache cases of "[Feature][KV Connector] Support QSA HiSparse
+ * in disaggregated serving", Validation.  Reading of the slot layout:
+ *   Main slot (1152 bytes) = 512 latent bf16 | 64 rope bf16, little-endian,
+ *   at s * 1152;  Indexer slot (256 bytes) = 128 bf16 at s * 256.
+ */
+#define KVO_MAIN_SLOT_BF16 1152
+#define KVO_IDX_SLOT_BF16 256
+
+int64_t kvo_store_mla_bf16(const uint16_t *kv_latent, int64_t latent_stride,
+                           const uint16_t *k_rope, int64_t rope_stride,
+                           const uint16_t *index_k, int64_t index_stride,
+                           const int64_t *slot_mapping, int64_t num_tokens,
+                           uint8_t *const *main_caches,
+                           uint8_t *const *indexer_caches, int num_replicas,
+                           int64_t num_blocks, int64_t *invalid_out) {
+    int64_t num_slots = num_blocks * KVO_BLOCK;
+    int64_t written = 0, invalid = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (!slot_is_written(s, num_slots)) {
+            if (s != -1) ++invalid;
+            continue;
+        }
+        for (int r = 0; r < num_replicas; ++r) {
+            uint8_t *m = main_caches[r] + s * KVO_MAIN_SLOT_BF16;
+            for (int i = 0; i < KVO_LATENT_DIM; ++i)
+                put_le16(m + 2 * i, kv_latent[t * latent_stride + i]);
+            for (int i = 0; i < KVO_ROPE_DIM; ++i)
+                put_le16(m + 2 * KVO_LATENT_DIM + 2 * i, k_rope[t * rope_stride + i]);
+            uint8_t *x = indexer_caches[r] + s * KVO_IDX_SLOT_BF16;
+            for (int i = 0; i < KVO_INDEXER_DIM; ++i)
+                put_le16(x + 2 * i, index_k[t * index_stride + i]);
+        }
+        ++written;
+    }
+    if (invalid_out) *invalid_out = invalid;
+    return written;
+}
