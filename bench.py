@@ -52,10 +52,12 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE = os.path.join(ROOT, "profiles", "store_mla_fp8_prefill_c4x3584.md")
 
 
-def store_bytes(num_tokens: int, num_valid: int, replicas: int) -> int:
+def store_bytes(num_tokens: int, num_valid: int, replicas: int, bf16_cache: bool = False) -> int:
     """Algorithmic HBM bytes of one store launch: slots + rows read once +
-    788 bytes per valid row and replica written."""
-    return 8 * num_tokens + num_valid * (ROW_IN + ROW_OUT * replicas)
+    the bytes written per valid row and replica (788 for the fp8 cache,
+    1408 for the unquantised bf16 cache)."""
+    out = ROW_IN if bf16_cache else ROW_OUT
+    return 8 * num_tokens + num_valid * (ROW_IN + out * replicas)
 
 
 # ------------------------------------------------------------------ helpers
@@ -165,9 +167,10 @@ class Spec:
     own inputs and caches (distinct buffers, so a step's working set is
     larger than L2), every launch followed by an epoch advance."""
 
-    def __init__(self, name, layers, make, replicas, num_blocks, note):
+    def __init__(self, name, layers, make, replicas, num_blocks, note, bf16_cache=False):
         self.name, self.layers, self.make = name, layers, make
         self.replicas, self.num_blocks, self.note = replicas, num_blocks, note
+        self.bf16_cache = bf16_cache
 
 
 def _copy_of(index):
@@ -191,6 +194,9 @@ SPECS = {
     "prefill_c4x3584_61layers": lambda: Spec(
         WORKLOAD, LAYERS, _prefill_layer_fn(), 4, 1024,
         "61 layers, seeds 3+layer, one shared slot_mapping"),
+    "prefill_c4x3584_61layers_bf16": lambda: Spec(
+        "prefill_c4x3584_61layers_bf16", LAYERS, _prefill_layer_fn(), 4, 1024,
+        "the 61-layer prefill into unquantised bf16 caches", bf16_cache=True),
     "prefill_c16x1024": lambda: Spec(
         "prefill_c16x1024", 8, _copy_of(2), 4, 4096,
         "8 buffer copies of the c16 x 1024 batch per step"),
@@ -227,9 +233,11 @@ class Step:
         self.host_slots = torch.from_numpy(np.stack([w.slot_mapping for w in ws])).pin_memory()
         self.slots = self.host_slots.to(dev)
         nb = spec.num_blocks
-        self.main = [[torch.full((nb * 64 * 656,), inputs.GUARD_BYTE, dtype=torch.uint8,
+        main_bytes = nb * 64 * (1152 if spec.bf16_cache else 656)
+        idx_bytes = nb * 64 * (256 if spec.bf16_cache else 132)
+        self.main = [[torch.full((main_bytes,), inputs.GUARD_BYTE, dtype=torch.uint8,
                                  device=dev) for _ in range(spec.replicas)] for _ in range(L)]
-        self.idx = [[torch.full((nb * 8448,), inputs.GUARD_BYTE, dtype=torch.uint8,
+        self.idx = [[torch.full((idx_bytes,), inputs.GUARD_BYTE, dtype=torch.uint8,
                                 device=dev) for _ in range(spec.replicas)] for _ in range(L)]
         self.epoch = torch.zeros(1, dtype=torch.int64, device=dev)
         self.invalid = torch.zeros(1, dtype=torch.int64, device=dev)
@@ -244,8 +252,9 @@ class Step:
 
     def launch_layer(self, layer: int, with_epoch: bool = True):
         lat, rope, idx = self.views(layer)
-        kvpub.store_mla_fp8(lat, rope, idx, self.slots[layer], self.main[layer],
-                            self.idx[layer], self.spec.num_blocks, invalid_count=self.invalid)
+        store = kvpub.store_mla_bf16 if self.spec.bf16_cache else kvpub.store_mla_fp8
+        store(lat, rope, idx, self.slots[layer], self.main[layer], self.idx[layer],
+              self.spec.num_blocks, invalid_count=self.invalid)
         if with_epoch:
             kvpub.epoch_advance(self.epoch)
 
@@ -384,7 +393,7 @@ def run_ours(args):
 
     rows_x_r = sum(step.valid) * Rr
     value = whole_job_rate(world, rows_x_r, ms_per_step)
-    launch_bytes = [store_bytes(step.num_tokens, v, Rr) for v in step.valid]
+    launch_bytes = [store_bytes(step.num_tokens, v, Rr, spec.bf16_cache) for v in step.valid]
     per_launch = sum(launch_bytes) / L
     peak, peak_kind = measured_peak()
     kernel_ms = store_ms / (args.steps * L)
@@ -394,7 +403,7 @@ def run_ours(args):
     traffic = profiled_traffic() if spec.name == WORKLOAD else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": f"store_mla_fp8_kernel<{Rr}>",
+                "kernel": f"store_mla_{'bf16' if spec.bf16_cache else 'fp8'}_kernel<{Rr}>",
                 "algorithmic_bytes": int(round(per_launch)),
                 "kernel_us": round(kernel_ms * 1e3, 2), "peak_source": f"{peak_kind} hbm_gbs",
                 "timing": timing}

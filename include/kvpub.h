@@ -82,6 +82,8 @@ typedef enum {
 #define KVPUB_INDEXER_SLOT_BYTES 132
 #define KVPUB_INDEXER_BLOCK_BYTES (KVPUB_BLOCK_SIZE * KVPUB_INDEXER_SLOT_BYTES)
 #define KVPUB_GATHER_ROW_BYTES 1408  /* (512 + 64 + 128) bf16 */
+#define KVPUB_MAIN_SLOT_BYTES_BF16 1152     /* (512 + 64) bf16 */
+#define KVPUB_INDEXER_SLOT_BYTES_BF16 256   /* 128 bf16 */
 #define KVPUB_MAX_POLLS (1ull << 24)
 #define KVPUB_STATIC_GATHER_MAX_TOKENS 4096
 
@@ -114,6 +116,32 @@ typedef enum {
  *                the number of invalid (not -1, out-of-range) slots to it.
  */
 kvpub_status kvpub_store_mla_fp8(
+    const void *kv_latent, int64_t latent_stride,
+    const void *k_rope, int64_t rope_stride,
+    const void *index_k, int64_t index_stride,
+    const int64_t *slot_mapping, int64_t num_tokens,
+    void *const *main_caches, void *const *indexer_caches, int num_replicas,
+    int64_t num_blocks, int block_size,
+    unsigned long long *invalid_count, kvpub_stream_t stream);
+
+/*
+ * Unquantised (bf16) cache variant of the same publication. It has the same
+ * rows, slots, replicas, launch and failure rules as kvpub_store_mla_fp8,
+ * but the bytes are stored as they arrive, with no scales. Source: the BF16
+ * main/indexer cache cases listed under Validation on "[Feature][KV
+ * Connector] Support QSA HiSparse in disaggregated serving", published as
+ * on "[Kernel][PCP] Publish replicated KV updates through PyTorch symmetric
+ * memory", Summary.
+ *
+ * Layout (a reading; the pages give none):
+ *  - Main cache r: num_blocks * 64 slots of KVPUB_MAIN_SLOT_BYTES_BF16 =
+ *    1152 bytes. Slot s at byte s * 1152 holds the 512 latent bf16 values,
+ *    then the 64 rope bf16 values.
+ *  - Indexer cache r: slots of KVPUB_INDEXER_SLOT_BYTES_BF16 = 256 bytes.
+ *    Slot s at byte s * 256 holds the 128 Indexer-K bf16 values.
+ * Arguments are as in kvpub_store_mla_fp8, with these cache sizes.
+ */
+kvpub_status kvpub_store_mla_bf16(
     const void *kv_latent, int64_t latent_stride,
     const void *k_rope, int64_t rope_stride,
     const void *index_k, int64_t index_stride,

@@ -64,6 +64,10 @@ __device__ __forceinline__ void st16(void *p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+__device__ __forceinline__ void st8(void *p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
 // Plain store, for the gather workspace that the insert launches read back.
 __device__ __forceinline__ void st16_keep(void *p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
@@ -148,10 +152,30 @@ __device__ __forceinline__ void publish_row(const StoreArgs &a, const RowRegs &v
     }
 }
 
+// Unquantised (bf16) cache variant: the row's bytes stored as they arrive.
+// Main slot s = latent | rope at s * 1152; Indexer slot s = index_k at
+// s * 256.  The lanes hold the row exactly as load_row left it.
+template <int R>
+__device__ __forceinline__ void copy_row_bf16(const StoreArgs &a, const RowRegs &v, int64_t s,
+                                              int lane) {
+    const int64_t main_off = s * KVPUB_MAIN_SLOT_BYTES_BF16 + 32 * lane;
+    const int64_t rope_off = s * KVPUB_MAIN_SLOT_BYTES_BF16 + 2 * KVPUB_LATENT_DIM +
+                             16 * (lane - 1);
+    const int64_t idx_off = s * KVPUB_INDEXER_SLOT_BYTES_BF16 + 8 * lane;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        uint8_t *m = a.rep.main[r];
+        st16(m + main_off, v.x0);
+        st16(m + main_off + 16, v.x1);
+        if (lane >= 1 && lane <= 8) st16(m + rope_off, v.tail);
+        st8(a.rep.indexer[r] + idx_off, v.xi);
+    }
+}
+
 // Grid-stride over token rows, one warp per row.  The next row's slot and
 // inputs are loaded before the current row is quantised, so each warp keeps
 // two rows of loads in flight.
-template <int R>
+template <int R, bool kFp8>
 __device__ __forceinline__ void publish_rows(const StoreArgs &a) {
     const int lane = threadIdx.x & 31;
     const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -169,7 +193,8 @@ __device__ __forceinline__ void publish_rows(const StoreArgs &a) {
             if (slot_written(s_next, a.num_slots)) load_row(a, t_next, lane, nxt);
         }
         if (slot_written(s, a.num_slots)) {
-            publish_row<R>(a, cur, s, lane);
+            if (kFp8) publish_row<R>(a, cur, s, lane);
+            else copy_row_bf16<R>(a, cur, s, lane);
         } else if (s != -1 && lane == 0 && a.invalid_count != nullptr) {
             atomicAdd(a.invalid_count, 1ull);
         }
@@ -182,7 +207,12 @@ __device__ __forceinline__ void publish_rows(const StoreArgs &a) {
 
 template <int R>
 __global__ void __launch_bounds__(kThreads) store_mla_fp8_kernel(const StoreArgs a) {
-    publish_rows<R>(a);
+    publish_rows<R, true>(a);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads) store_mla_bf16_kernel(const StoreArgs a) {
+    publish_rows<R, false>(a);
 }
 
 __device__ __forceinline__ void release_add_epoch(unsigned long long *epoch) {
@@ -194,7 +224,7 @@ template <int R>
 __global__ void __launch_bounds__(kThreads)
 store_mla_fp8_publish_kernel(const StoreArgs a, unsigned long long *epoch,
                              unsigned int *done_count) {
-    publish_rows<R>(a);
+    publish_rows<R, true>(a);
     __shared__ bool is_last;
     __threadfence();                      // this thread's stores, GPU-wide
     __syncthreads();
@@ -295,7 +325,7 @@ kvpub_status validate(const void *kv_latent, int64_t latent_stride, const void *
                       const int64_t *slot_mapping, int64_t num_tokens,
                       void *const *main_caches, void *const *indexer_caches, int num_replicas,
                       int64_t num_blocks, int block_size, unsigned long long *invalid_count,
-                      Validated *out) {
+                      Validated *out, int64_t main_slot_bytes = KVPUB_MAIN_SLOT_BYTES) {
     if (num_replicas < 1) return fail(KVPUB_ERR_INVALID_ARG, "num_replicas %d < 1", num_replicas);
     if (num_replicas > KVPUB_MAX_REPLICAS)
         return fail(KVPUB_ERR_TOO_MANY_REPLICAS, "num_replicas %d > %d", num_replicas,
@@ -305,7 +335,7 @@ kvpub_status validate(const void *kv_latent, int64_t latent_stride, const void *
     if (num_tokens < 0)
         return fail(KVPUB_ERR_INVALID_ARG, "num_tokens %lld < 0", (long long)num_tokens);
     if (num_blocks < 1 ||
-        num_blocks > INT64_MAX / (KVPUB_BLOCK_SIZE * (int64_t)KVPUB_MAIN_SLOT_BYTES))
+        num_blocks > INT64_MAX / (KVPUB_BLOCK_SIZE * main_slot_bytes))
         return fail(KVPUB_ERR_INVALID_ARG, "num_blocks %lld out of range", (long long)num_blocks);
     if (main_caches == nullptr || indexer_caches == nullptr)
         return fail(KVPUB_ERR_INVALID_ARG, "cache pointer arrays are NULL");
@@ -437,6 +467,21 @@ template <int R>
 std::atomic<int> LaunchStore<R>::resident[kMaxDevices];
 
 template <int R>
+struct LaunchStoreBf16 {
+    static std::atomic<int> resident[kMaxDevices];
+    static kvpub_status go(cudaStream_t stream, const StoreArgs &a) {
+        int grid = 0;
+        kvpub_status st = one_wave_grid(store_mla_bf16_kernel<R>, resident, a.num_tokens, &grid);
+        if (st != KVPUB_OK) return st;
+        (void)cudaGetLastError();
+        store_mla_bf16_kernel<R><<<grid, kThreads, 0, stream>>>(a);
+        return launched("store_mla_bf16");
+    }
+};
+template <int R>
+std::atomic<int> LaunchStoreBf16<R>::resident[kMaxDevices];
+
+template <int R>
 struct LaunchPublish {
     static std::atomic<int> resident[kMaxDevices];
     static kvpub_status go(cudaStream_t stream, const StoreArgs &a, unsigned long long *epoch,
@@ -499,6 +544,21 @@ extern "C" kvpub_status kvpub_store_mla_fp8(
     if (st != KVPUB_OK) return st;
     if (num_tokens == 0) return ok();
     return dispatch_replicas<LaunchStore>(v.num_replicas, (cudaStream_t)stream, v.args);
+}
+
+extern "C" kvpub_status kvpub_store_mla_bf16(
+    const void *kv_latent, int64_t latent_stride, const void *k_rope, int64_t rope_stride,
+    const void *index_k, int64_t index_stride, const int64_t *slot_mapping, int64_t num_tokens,
+    void *const *main_caches, void *const *indexer_caches, int num_replicas, int64_t num_blocks,
+    int block_size, unsigned long long *invalid_count, kvpub_stream_t stream) {
+    Validated v;
+    kvpub_status st = validate(kv_latent, latent_stride, k_rope, rope_stride, index_k,
+                               index_stride, slot_mapping, num_tokens, main_caches,
+                               indexer_caches, num_replicas, num_blocks, block_size,
+                               invalid_count, &v, KVPUB_MAIN_SLOT_BYTES_BF16);
+    if (st != KVPUB_OK) return st;
+    if (num_tokens == 0) return ok();
+    return dispatch_replicas<LaunchStoreBf16>(v.num_replicas, (cudaStream_t)stream, v.args);
 }
 
 extern "C" kvpub_status kvpub_store_mla_fp8_publish(

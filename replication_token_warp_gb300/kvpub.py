@@ -7,7 +7,8 @@ non-zero status.  There is no fallback: if the library is not built, the
 first call raises.
 
 Names follow the C ABI in include/kvpub.h: ``store_mla_fp8`` (fused direct
-publication into every replica), ``store_mla_fp8_publish`` (the same store
+publication into every replica), ``store_mla_bf16`` (the unquantised cache
+variant), ``store_mla_fp8_publish`` (the same store
 plus the device-epoch advance, one launch), ``gather_insert`` (the unfused
 gather-then-insert path), ``epoch_advance`` and ``epoch_wait``.
 """
@@ -29,6 +30,8 @@ BLOCK_SIZE = 64
 MAIN_SLOT_BYTES = 656
 INDEXER_BLOCK_BYTES = BLOCK_SIZE * 132
 GATHER_ROW_BYTES = 1408
+MAIN_SLOT_BYTES_BF16 = 1152
+INDEXER_SLOT_BYTES_BF16 = 256
 MAX_REPLICAS = 8
 MAX_POLLS = 1 << 24
 STATIC_GATHER_MAX_TOKENS = 4096
@@ -56,6 +59,7 @@ _STORE_ARGS = [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
 SIGNATURES = {
     "kvpub_store_mla_fp8": (_STORE_ARGS + [_vp], ctypes.c_int),
     "kvpub_store_mla_fp8_publish": (_STORE_ARGS + [_vp, _vp, _vp], ctypes.c_int),
+    "kvpub_store_mla_bf16": (_STORE_ARGS + [_vp], ctypes.c_int),
     "kvpub_gather_workspace_bytes": ([_i64], ctypes.c_size_t),
     "kvpub_gather_insert": (_STORE_ARGS + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "kvpub_gather_insert_noalloc": (_STORE_ARGS + [_vp], ctypes.c_int),
@@ -120,23 +124,24 @@ def _ptr_array(ts):
     return arr
 
 
-def _caches(main_caches, indexer_caches, num_blocks):
+def _caches(main_caches, indexer_caches, num_blocks, main_slot=MAIN_SLOT_BYTES,
+            indexer_block=INDEXER_BLOCK_BYTES):
     if len(main_caches) != len(indexer_caches):
         raise ValueError("need as many Indexer caches as Main caches")
     for c in list(main_caches) + list(indexer_caches):
         if not c.is_cuda or c.dtype != torch.uint8 or not c.is_contiguous():
             raise ValueError("caches are contiguous uint8 CUDA tensors")
     if num_blocks is None:
-        num_blocks = main_caches[0].numel() // (BLOCK_SIZE * MAIN_SLOT_BYTES)
+        num_blocks = main_caches[0].numel() // (BLOCK_SIZE * main_slot)
     for m, ix in zip(main_caches, indexer_caches):
-        if (m.numel() < num_blocks * BLOCK_SIZE * MAIN_SLOT_BYTES
-                or ix.numel() < num_blocks * INDEXER_BLOCK_BYTES):
+        if (m.numel() < num_blocks * BLOCK_SIZE * main_slot
+                or ix.numel() < num_blocks * indexer_block):
             raise ValueError(f"a cache is smaller than {num_blocks} blocks")
     return _ptr_array(main_caches), _ptr_array(indexer_caches), int(num_blocks)
 
 
 def _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
-                num_blocks, invalid_count):
+                num_blocks, invalid_count, bf16_cache=False):
     if slot_mapping.dtype != torch.int64 or slot_mapping.dim() != 1 or not slot_mapping.is_cuda:
         raise ValueError("slot_mapping: expected a 1-D int64 CUDA tensor")
     if not slot_mapping.is_contiguous():
@@ -145,7 +150,11 @@ def _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_c
     lp, ls = _rows(kv_latent, LATENT_DIM, T, "kv_latent")
     rp, rs = _rows(k_rope, ROPE_DIM, T, "k_rope")
     ip, is_ = _rows(index_k, INDEXER_DIM, T, "index_k")
-    mains, idxs, nb = _caches(main_caches, indexer_caches, num_blocks)
+    if bf16_cache:
+        mains, idxs, nb = _caches(main_caches, indexer_caches, num_blocks, MAIN_SLOT_BYTES_BF16,
+                                  BLOCK_SIZE * INDEXER_SLOT_BYTES_BF16)
+    else:
+        mains, idxs, nb = _caches(main_caches, indexer_caches, num_blocks)
     cnt = None
     if invalid_count is not None:
         if invalid_count.dtype not in (torch.int64, torch.uint64) or not invalid_count.is_cuda:
@@ -161,6 +170,15 @@ def store_mla_fp8(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer
     args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
                        num_blocks, invalid_count)
     check(lib().kvpub_store_mla_fp8(*args, _stream_handle(stream)))
+
+
+def store_mla_bf16(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                   num_blocks=None, invalid_count=None, stream=None) -> None:
+    """Unquantised variant: every row's bf16 bytes into all replicas
+    (Main slot 1152 B, Indexer slot 256 B)."""
+    args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                       num_blocks, invalid_count, bf16_cache=True)
+    check(lib().kvpub_store_mla_bf16(*args, _stream_handle(stream)))
 
 
 def store_mla_fp8_publish(kv_latent, k_rope, index_k, slot_mapping, main_caches,

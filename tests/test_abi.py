@@ -42,7 +42,8 @@ def declared_functions():
 
 
 def test_header_declares_the_entry_points():
-    want = {"kvpub_store_mla_fp8", "kvpub_store_mla_fp8_publish", "kvpub_gather_insert",
+    want = {"kvpub_store_mla_fp8", "kvpub_store_mla_fp8_publish", "kvpub_store_mla_bf16",
+            "kvpub_gather_insert",
             "kvpub_gather_workspace_bytes", "kvpub_epoch_advance", "kvpub_epoch_wait",
             "kvpub_last_error"}
     assert want <= declared_functions()
@@ -106,6 +107,7 @@ def test_store_rejects_bad_arguments(lib, name, over, status):
     assert kvpub.last_error() != ""
     assert lib.kvpub_gather_insert(*store_args(**over), A, 10 ** 9, None) == status
     assert lib.kvpub_store_mla_fp8_publish(*store_args(**over), A, A, None) == status
+    assert lib.kvpub_store_mla_bf16(*store_args(**over), None) == status
 
 
 def test_gather_rejects_small_or_missing_workspace(lib):
