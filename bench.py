@@ -206,6 +206,9 @@ SPECS = {
     "capacity_706624_x1": lambda: Spec(
         "capacity_706624_x1", 1, _copy_of(4), 4, 11041,
         "one copy of the capacity batch (profiling case, ~2.3 GB)"),
+    "capacity_706624_bf16": lambda: Spec(
+        "capacity_706624_bf16", 4, _copy_of(4), 4, 11041,
+        "4 buffer copies of the capacity batch, unquantised bf16 caches", bf16_cache=True),
     "stress_131072": lambda: Spec(
         "stress_131072", 1, _stress, 4, 8192,
         "one 131,072-row launch (profiling case)"),

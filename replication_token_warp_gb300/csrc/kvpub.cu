@@ -225,16 +225,21 @@ __global__ void __launch_bounds__(kThreads)
 store_mla_fp8_publish_kernel(const StoreArgs a, unsigned long long *epoch,
                              unsigned int *done_count) {
     publish_rows<R, true>(a);
+    // The barrier orders every thread's stores before thread 0's counter
+    // update; that update is an acq_rel atomic at GPU scope, so it releases
+    // the whole block's stores and, in the last block, acquires every other
+    // block's.  (The same barrier-then-one-thread pattern as a grid-wide
+    // sync, with the fence folded into the atomic.)
     __shared__ bool is_last;
-    __threadfence();                      // this thread's stores, GPU-wide
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned int prev = atomicAdd(done_count, 1u);
+        unsigned int prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev) : "l"(done_count) : "memory");
         is_last = (prev == gridDim.x - 1);
     }
     __syncthreads();
     if (is_last && threadIdx.x == 0) {
-        __threadfence();                  // acquire every block's stores
         atomicExch(done_count, 0u);       // ready for the next call / replay
         release_add_epoch(epoch);
     }
