@@ -52,6 +52,13 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE = os.path.join(ROOT, "profiles", "store_mla_fp8_prefill_c4x3584.md")
 
 
+def gather_insert_bytes(num_tokens: int, num_valid: int, replicas: int) -> int:
+    """Algorithmic HBM bytes of the unfused path for one layer: the gather
+    copies every row (read + write 1408 B), then each replica's insert reads
+    the slots and the gathered rows and writes 788 B per valid row."""
+    return 2 * ROW_IN * num_tokens + replicas * (8 * num_tokens + num_valid * (ROW_IN + ROW_OUT))
+
+
 def store_bytes(num_tokens: int, num_valid: int, replicas: int, bf16_cache: bool = False) -> int:
     """Algorithmic HBM bytes of one store launch: slots + rows read once +
     the bytes written per valid row and replica (788 for the fp8 cache,
@@ -203,6 +210,9 @@ SPECS = {
     "capacity_706624": lambda: Spec(
         "capacity_706624", 4, _copy_of(4), 4, 11041,
         "4 buffer copies of the 706,624-slot capacity batch per step"),
+    "decode_c64_61layers": lambda: Spec(
+        "decode_c64_61layers", LAYERS, _copy_of(1), 2, 2048,
+        "a 64-sequence decode batch published in each of 61 layers (latency-bound)"),
     "capacity_706624_x1": lambda: Spec(
         "capacity_706624_x1", 1, _copy_of(4), 4, 11041,
         "one copy of the capacity batch (profiling case, ~2.3 GB)"),
@@ -220,8 +230,8 @@ class Step:
     (latent | rope | Indexer-K as strided views), a slot_mapping and R
     replica caches per layer, one epoch counter."""
 
-    def __init__(self, dev, spec: Spec):
-        self.dev, self.spec = dev, spec
+    def __init__(self, dev, spec: Spec, path: str = "direct"):
+        self.dev, self.spec, self.path = dev, spec, path
         L = spec.layers
         ws = [spec.make(layer) for layer in range(L)]
         T = ws[0].num_tokens
@@ -244,6 +254,14 @@ class Step:
                                 device=dev) for _ in range(spec.replicas)] for _ in range(L)]
         self.epoch = torch.zeros(1, dtype=torch.int64, device=dev)
         self.invalid = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.workspace = None
+        if path == "gather":
+            self.workspace = torch.empty(kvpub.gather_workspace_bytes(T), dtype=torch.uint8,
+                                         device=dev)
+
+    def launches_per_layer(self, with_epoch: bool = True) -> int:
+        n = 1 + self.spec.replicas if self.path == "gather" else 1
+        return n + (1 if with_epoch else 0)
 
     def views(self, layer):
         x = self.rows[layer]
@@ -255,9 +273,14 @@ class Step:
 
     def launch_layer(self, layer: int, with_epoch: bool = True):
         lat, rope, idx = self.views(layer)
-        store = kvpub.store_mla_bf16 if self.spec.bf16_cache else kvpub.store_mla_fp8
-        store(lat, rope, idx, self.slots[layer], self.main[layer], self.idx[layer],
-              self.spec.num_blocks, invalid_count=self.invalid)
+        if self.path == "gather":
+            kvpub.gather_insert(lat, rope, idx, self.slots[layer], self.main[layer],
+                                self.idx[layer], self.workspace, self.spec.num_blocks,
+                                invalid_count=self.invalid)
+        else:
+            store = kvpub.store_mla_bf16 if self.spec.bf16_cache else kvpub.store_mla_fp8
+            store(lat, rope, idx, self.slots[layer], self.main[layer], self.idx[layer],
+                  self.spec.num_blocks, invalid_count=self.invalid)
         if with_epoch:
             kvpub.epoch_advance(self.epoch)
 
@@ -380,7 +403,9 @@ def run_ours(args):
     kbuild.build()
     kvpub.lib()
     spec = SPECS[args.workload]()
-    step = Step(dev, spec)
+    if args.path == "gather" and spec.bf16_cache:
+        raise SystemExit("the gather-then-insert path exists for the fp8 cache only")
+    step = Step(dev, spec, args.path)
     L, Rr = spec.layers, spec.replicas
     g = step.capture(with_epoch=True)
     g_store = step.capture(with_epoch=False)
@@ -396,17 +421,22 @@ def run_ours(args):
 
     rows_x_r = sum(step.valid) * Rr
     value = whole_job_rate(world, rows_x_r, ms_per_step)
-    launch_bytes = [store_bytes(step.num_tokens, v, Rr, spec.bf16_cache) for v in step.valid]
+    if args.path == "gather":
+        launch_bytes = [gather_insert_bytes(step.num_tokens, v, Rr) for v in step.valid]
+        kernel_name = f"gather_rows_kernel + {Rr} x store_mla_fp8_kernel<1> (per layer)"
+    else:
+        launch_bytes = [store_bytes(step.num_tokens, v, Rr, spec.bf16_cache) for v in step.valid]
+        kernel_name = f"store_mla_{'bf16' if spec.bf16_cache else 'fp8'}_kernel<{Rr}>"
     per_launch = sum(launch_bytes) / L
     peak, peak_kind = measured_peak()
     kernel_ms = store_ms / (args.steps * L)
-    timing = (f"CUDA events around {args.steps} replays of a graph of the same {L} store "
-              f"launches (no epoch kernels) / {args.steps * L} launches, gaps included")
+    timing = (f"CUDA events around {args.steps} replays of a graph of the same {L} layers' "
+              f"store launches (no epoch kernels) / {args.steps * L} layers, gaps included")
     achieved = per_launch / (kernel_ms / 1e3) / 1e9
-    traffic = profiled_traffic() if spec.name == WORKLOAD else None
+    traffic = profiled_traffic() if (spec.name == WORKLOAD and args.path == "direct") else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": f"store_mla_{'bf16' if spec.bf16_cache else 'fp8'}_kernel<{Rr}>",
+                "kernel": kernel_name,
                 "algorithmic_bytes": int(round(per_launch)),
                 "kernel_us": round(kernel_ms * 1e3, 2), "peak_source": f"{peak_kind} hbm_gbs",
                 "timing": timing}
@@ -427,14 +457,15 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": spec.name, "layers": L, "rows_per_layer": step.num_tokens,
                    "valid_rows_per_layer": step.valid[0], "replicas": Rr,
-                   "blocks_per_replica": spec.num_blocks, "launches_per_step": 2 * L,
+                   "blocks_per_replica": spec.num_blocks,
+                   "launches_per_step": step.launches_per_layer() * L, "path": args.path,
                    "graph": True, "parallelism": f"replicas only x{world}", "note": spec.note,
                    "l2": "inputs larger than L2: one step touches "
                          f"{sum(launch_bytes) / 1e9:.2f} GB",
                    "hbm_gbs_step": round(sum(launch_bytes) / (ms_per_step / 1e3) / 1e9, 1)},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": 2 * L * args.steps,
+        "gpu_launches": step.launches_per_layer() * L * args.steps,
         "clocks": clocks.summary(t0, t1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -496,6 +527,9 @@ def main():
                     help="seconds of oracle work for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", choices=["direct", "gather"], default="direct",
+                    help="direct publication (the measured line) or the unfused "
+                         "gather-then-insert path, for comparison")
     ap.add_argument("--workload", choices=sorted(SPECS), default=WORKLOAD,
                     help="the default is the measured line; the others are for "
                          "per-workload roofline figures and ncu captures")
