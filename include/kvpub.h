@@ -14,11 +14,16 @@
  *  - Every pointer argument is a device pointer unless its comment says
  *    "host".
  *  - The caller owns and allocates all memory: inputs, caches, workspace and
- *    counters. These entry points allocate nothing, never synchronise, and
- *    keep no state except the calling thread's last error message.
+ *    counters. The one exception is kvpub_gather_insert_noalloc, whose
+ *    workspace is a fixed array inside the library. These entry points
+ *    allocate nothing and never synchronise. Their only state is the calling
+ *    thread's last error message and, per device, cached launch geometry
+ *    (SM count, resident blocks per kernel).
  *  - Work is enqueued on `stream`. NULL means the legacy default stream.
- *  - Every call may be captured into a CUDA graph. Kernel parameters hold
- *    the pointers by value, so a replay reuses the same buffers.
+ *  - kvpub_store_mla_fp8, kvpub_store_mla_bf16, kvpub_store_mla_fp8_publish,
+ *    kvpub_gather_insert, kvpub_epoch_advance and kvpub_epoch_wait may be
+ *    captured into a CUDA graph. Kernel parameters hold the pointers by
+ *    value, so a replay reuses the same buffers.
  *  - Validation is fail-closed. Every check runs on the host before
  *    anything is enqueued. On any error nothing is launched, no byte
  *    changes, and kvpub_last_error() says why.
