@@ -78,6 +78,15 @@ __device__ __forceinline__ void st4(void *p, uint32_t v) {
     asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
+// Every kernel here is launched with programmatic stream serialization, so
+// its blocks may be scheduled while the previous kernel on the stream is
+// still finishing.  Each kernel's first instruction waits until that kernel
+// has completed and its memory is visible, so nothing is read or written
+// out of stream order; only the launch latency overlaps.
+__device__ __forceinline__ void wait_previous_kernel() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // One token row's inputs as this lane holds them.
 struct RowRegs {
     uint4 x0, x1;   // latent elements [16 l, 16 l + 16)
@@ -207,11 +216,13 @@ __device__ __forceinline__ void publish_rows(const StoreArgs &a) {
 
 template <int R>
 __global__ void __launch_bounds__(kThreads) store_mla_fp8_kernel(const StoreArgs a) {
+    wait_previous_kernel();
     publish_rows<R, true>(a);
 }
 
 template <int R>
 __global__ void __launch_bounds__(kThreads) store_mla_bf16_kernel(const StoreArgs a) {
+    wait_previous_kernel();
     publish_rows<R, false>(a);
 }
 
@@ -224,6 +235,7 @@ template <int R>
 __global__ void __launch_bounds__(kThreads)
 store_mla_fp8_publish_kernel(const StoreArgs a, unsigned long long *epoch,
                              unsigned int *done_count) {
+    wait_previous_kernel();
     publish_rows<R, true>(a);
     // The barrier orders every thread's stores before thread 0's counter
     // update; that update is an acq_rel atomic at GPU scope, so it releases
@@ -249,6 +261,7 @@ store_mla_fp8_publish_kernel(const StoreArgs a, unsigned long long *epoch,
 // 1408-byte workspace row (latent | rope | index_k).
 __global__ void __launch_bounds__(kThreads)
 gather_rows_kernel(const StoreArgs a, uint8_t *workspace) {
+    wait_previous_kernel();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -268,11 +281,13 @@ gather_rows_kernel(const StoreArgs a, uint8_t *workspace) {
 }
 
 __global__ void epoch_advance_kernel(unsigned long long *epoch) {
+    wait_previous_kernel();
     release_add_epoch(epoch);
 }
 
 __global__ void epoch_wait_kernel(const unsigned long long *epoch, unsigned long long target,
                                   unsigned long long max_polls, unsigned int *status) {
+    wait_previous_kernel();
     unsigned int st = 1u;
     for (unsigned long long i = 0; i < max_polls; ++i) {
         unsigned long long v;
@@ -442,6 +457,23 @@ kvpub_status launched(const char *what) {
     return ok();
 }
 
+// Launch with programmatic stream serialization (see wait_previous_kernel).
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), int grid, int threads, cudaStream_t stream,
+                   Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <template <int> class Launch, typename... Args>
 kvpub_status dispatch_replicas(int r, Args &&...args) {
     switch (r) {
@@ -464,7 +496,7 @@ struct LaunchStore {
         kvpub_status st = one_wave_grid(store_mla_fp8_kernel<R>, resident, a.num_tokens, &grid);
         if (st != KVPUB_OK) return st;
         (void)cudaGetLastError();
-        store_mla_fp8_kernel<R><<<grid, kThreads, 0, stream>>>(a);
+        (void)launch(store_mla_fp8_kernel<R>, grid, kThreads, stream, a);
         return launched("store_mla_fp8");
     }
 };
@@ -479,7 +511,7 @@ struct LaunchStoreBf16 {
         kvpub_status st = one_wave_grid(store_mla_bf16_kernel<R>, resident, a.num_tokens, &grid);
         if (st != KVPUB_OK) return st;
         (void)cudaGetLastError();
-        store_mla_bf16_kernel<R><<<grid, kThreads, 0, stream>>>(a);
+        (void)launch(store_mla_bf16_kernel<R>, grid, kThreads, stream, a);
         return launched("store_mla_bf16");
     }
 };
@@ -496,7 +528,7 @@ struct LaunchPublish {
             one_wave_grid(store_mla_fp8_publish_kernel<R>, resident, a.num_tokens, &grid);
         if (st != KVPUB_OK) return st;
         (void)cudaGetLastError();
-        store_mla_fp8_publish_kernel<R><<<grid, kThreads, 0, stream>>>(a, epoch, done);
+        (void)launch(store_mla_fp8_publish_kernel<R>, grid, kThreads, stream, a, epoch, done);
         return launched("store_mla_fp8_publish");
     }
 };
@@ -513,7 +545,7 @@ kvpub_status gather_then_insert(const Validated &v, uint8_t *ws, cudaStream_t s)
     kvpub_status st = one_wave_grid(gather_rows_kernel, g_gather_resident, v.args.num_tokens, &grid);
     if (st != KVPUB_OK) return st;
     (void)cudaGetLastError();
-    gather_rows_kernel<<<grid, kThreads, 0, s>>>(v.args, ws);
+    (void)launch(gather_rows_kernel, grid, kThreads, s, v.args, ws);
     if ((st = launched("gather_rows")) != KVPUB_OK) return st;
     StoreArgs ins = v.args;
     const uint16_t *w16 = reinterpret_cast<const uint16_t *>(ws);
@@ -617,7 +649,7 @@ extern "C" kvpub_status kvpub_epoch_advance(unsigned long long *epoch, kvpub_str
     if (epoch == nullptr) return fail(KVPUB_ERR_INVALID_ARG, "epoch is NULL");
     if (!aligned(epoch, 8)) return fail(KVPUB_ERR_ALIGNMENT, "epoch is not 8-byte aligned");
     (void)cudaGetLastError();
-    epoch_advance_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(epoch);
+    (void)launch(epoch_advance_kernel, 1, 1, (cudaStream_t)stream, epoch);
     return launched("epoch_advance");
 }
 
@@ -633,7 +665,7 @@ extern "C" kvpub_status kvpub_epoch_wait(const unsigned long long *epoch,
         return fail(KVPUB_ERR_INVALID_ARG, "max_polls %llu outside [1, %llu]", max_polls,
                     kMaxPolls);
     (void)cudaGetLastError();
-    epoch_wait_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(epoch, target, max_polls, status);
+    (void)launch(epoch_wait_kernel, 1, 1, (cudaStream_t)stream, epoch, target, max_polls, status);
     return launched("epoch_wait");
 }
 
