@@ -262,3 +262,26 @@ def test_failures_change_nothing(dev):
     torch.cuda.synchronize()
     main, idx = c.host()
     assert np.all(main[0] == w.guard) and np.all(idx[0] == w.guard)
+
+
+def test_store_sees_the_producer_kernel_that_precedes_it(dev):
+    """Every kernel here may be scheduled early (programmatic dependent
+    launch) but waits for the previous kernel on the stream before touching
+    memory.  A torch kernel rewrites the input rows right before each store;
+    the stores must see the new rows, round after round."""
+    ws = [inputs.random_rows(seed=900 + k, num_tokens=2048, num_blocks=40, num_replicas=2)
+          for k in range(3)]
+    slots = ws[0].slot_mapping
+    for w in ws:
+        w.slot_mapping = slots
+    src = [DevInputs(w, dev) for w in ws]
+    x = DevInputs(ws[0], dev)
+    c = Caches(2, ws[0].num_blocks, ws[0].guard, dev)
+    for rnd in range(6):
+        w, y = ws[rnd % 3], src[rnd % 3]
+        x.lat.copy_(y.lat)
+        x.rope.copy_(y.rope)
+        x.idx.copy_(y.idx)
+        kvpub.store_mla_fp8(x.lat, x.rope, x.idx, x.slots, c.main, c.idx)
+        torch.cuda.synchronize()
+        assert_matches_oracle(c, *oracle_caches(w)[:2])
