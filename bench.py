@@ -319,6 +319,32 @@ class Step:
         return g
 
 
+def check_direct_equals_gather(step: Step):
+    """Before any timing: layer 0 published directly must leave the same
+    bytes as the unfused gather-then-insert path on the same inputs ("byte-
+    exact against gather-then-insert oracles before timing", as on
+    "[Kernel][PCP] Publish replicated KV updates through PyTorch symmetric
+    memory", Correctness and current-head validation)."""
+    if step.spec.bf16_cache:
+        return None
+    lat, rope, idx = step.views(0)
+    nb = step.spec.num_blocks
+    direct_main = [torch.full_like(c, inputs.GUARD_BYTE) for c in step.main[0]]
+    direct_idx = [torch.full_like(c, inputs.GUARD_BYTE) for c in step.idx[0]]
+    kvpub.store_mla_fp8(lat, rope, idx, step.slots[0], direct_main, direct_idx, nb)
+    gather_main = [torch.full_like(c, inputs.GUARD_BYTE) for c in step.main[0]]
+    gather_idx = [torch.full_like(c, inputs.GUARD_BYTE) for c in step.idx[0]]
+    ws = torch.empty(kvpub.gather_workspace_bytes(step.num_tokens), dtype=torch.uint8,
+                     device=step.dev)
+    kvpub.gather_insert(lat, rope, idx, step.slots[0], gather_main, gather_idx, ws, nb)
+    torch.cuda.synchronize()
+    same = all(torch.equal(a, b) for a, b in zip(direct_main + direct_idx,
+                                                 gather_main + gather_idx))
+    if not same:
+        raise RuntimeError("direct publication and gather-then-insert disagree on layer 0")
+    return True
+
+
 def time_graph(g, steps, warmup):
     for _ in range(warmup):
         g.replay()
@@ -407,6 +433,7 @@ def run_ours(args):
         raise SystemExit("the gather-then-insert path exists for the fp8 cache only")
     step = Step(dev, spec, args.path)
     L, Rr = spec.layers, spec.replicas
+    checked = check_direct_equals_gather(step)
     g = step.capture(with_epoch=True)
     g_store = step.capture(with_epoch=False)
     with ClockSampler(local) as clocks:
@@ -460,6 +487,7 @@ def run_ours(args):
                    "blocks_per_replica": spec.num_blocks,
                    "launches_per_step": step.launches_per_layer() * L, "path": args.path,
                    "graph": True, "parallelism": f"replicas only x{world}", "note": spec.note,
+                   "direct_equals_gather_before_timing": checked,
                    "l2": "inputs larger than L2: one step touches "
                          f"{sum(launch_bytes) / 1e9:.2f} GB",
                    "hbm_gbs_step": round(sum(launch_bytes) / (ms_per_step / 1e3) / 1e9, 1)},
