@@ -285,3 +285,11 @@ def test_store_sees_the_producer_kernel_that_precedes_it(dev):
         kvpub.store_mla_fp8(x.lat, x.rope, x.idx, x.slots, c.main, c.idx)
         torch.cuda.synchronize()
         assert_matches_oracle(c, *oracle_caches(w)[:2])
+
+
+def test_large_batch_matches_oracle(dev):
+    """131,072 rows (128 prefill requests x 1,024 tokens) into 4 replicas of
+    8,192-block caches: many rows per warp, the whole buffers byte-exact."""
+    w = inputs.prefill_batch(1000, 128, 1024, 8192)
+    c = run_store(w, dev, "fused")
+    assert_matches_oracle(c, *oracle_caches(w)[:2])
