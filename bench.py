@@ -391,13 +391,24 @@ def e2e_measure(step: Step, steps: int, warmup: int):
     h2d = step.host_rows.numel() * 2 + step.host_slots.numel() * 8
     d2h = 8
     g = step.capture_end_to_end()
+    # the transfer floor: this machine's host->device rate for the same bytes
+    for _ in range(2):
+        step.rows.copy_(step.host_rows, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        step.rows.copy_(step.host_rows, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    h2d_gbs = 3 * step.host_rows.numel() * 2 / e0.elapsed_time(e1) / 1e6
     before = int(step.epoch.item())
     ms, _, _ = time_graph(g, steps, warmup)
     after = int(step.host_epoch.item())
     if after != before + step.spec.layers * (warmup + steps):
         raise RuntimeError(f"end-to-end epoch read back {after}, expected "
                            f"{before + step.spec.layers * (warmup + steps)}")
-    return ms, h2d, d2h
+    return ms, h2d, d2h, h2d_gbs
 
 
 def cpu_baseline(budget_s: float):
@@ -471,11 +482,15 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 50))
-        e2e_ms, h2d, d2h = e2e_measure(step, e2e_steps, max(1, min(args.warmup, 3)))
+        e2e_ms, h2d, d2h, h2d_gbs = e2e_measure(step, e2e_steps, max(1, min(args.warmup, 3)))
         e2e_ms = max_over_ranks(e2e_ms)
+        floor_ms = h2d / (h2d_gbs * 1e6)
         e2e = {"value": whole_job_rate(world, rows_x_r, e2e_ms / e2e_steps), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps}
+               "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
+               "h2d_gbs_measured": round(h2d_gbs, 1),
+               "transfer_floor_ms": round(floor_ms, 4),
+               "frac_of_transfer_floor": round(floor_ms / (e2e_ms / e2e_steps), 4)}
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
