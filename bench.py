@@ -391,7 +391,7 @@ def e2e_measure(step: Step, steps: int, warmup: int):
     h2d = step.host_rows.numel() * 2 + step.host_slots.numel() * 8
     d2h = 8
     g = step.capture_end_to_end()
-    # the transfer floor: this box's host->device rate for the same bytes
+    # the transfer floor: this machine's host->device rate for the same bytes
     for _ in range(2):
         step.rows.copy_(step.host_rows, non_blocking=True)
     torch.cuda.synchronize()
