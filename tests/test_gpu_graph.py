@@ -149,3 +149,44 @@ def test_bench_step_matches_oracle(dev):
             assert np.array_equal(step.idx[layer][r].cpu().numpy(), want_idx[r])
     del step, g, ge
     torch.cuda.empty_cache()
+
+
+def test_every_capturable_call_replays_in_a_graph(dev):
+    """gather-then-insert, the bf16 store and the bounded wait, captured with
+    the epoch advance and replayed twice: bytes as the oracle's, epoch and
+    wait status as expected on every replay."""
+    import oracle
+    w = inputs.make(1)
+    from gpu_util import Caches, DevInputs
+    x = DevInputs(w, dev)
+    c_gather = Caches(2, w.num_blocks, w.guard, dev)
+    ws = torch.empty(kvpub.gather_workspace_bytes(w.num_tokens), dtype=torch.uint8, device=dev)
+    nb = w.num_blocks
+    main16 = [torch.full((nb * 64 * 1152,), w.guard, dtype=torch.uint8, device=dev) for _ in range(2)]
+    idx16 = [torch.full((nb * 64 * 256,), w.guard, dtype=torch.uint8, device=dev) for _ in range(2)]
+    epoch = torch.zeros(1, dtype=torch.int64, device=dev)
+    status = torch.full((1,), 7, dtype=torch.int32, device=dev)
+    scratch = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def step(ep, target):
+        kvpub.gather_insert(x.lat, x.rope, x.idx, x.slots, c_gather.main, c_gather.idx, ws, nb)
+        kvpub.store_mla_bf16(x.lat, x.rope, x.idx, x.slots, main16, idx16, nb)
+        kvpub.epoch_advance(ep)
+        kvpub.epoch_wait(ep, target, 1000, status)
+
+    step(scratch, 1)                              # load the kernels before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(epoch, 1)                            # reached on every replay: epoch >= 1
+    for k in (1, 2):
+        status.fill_(7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(epoch.item()) == k and int(status.item()) == 0
+    assert_matches_oracle(c_gather, *oracle_caches(w)[:2])
+    want16_main, want16_idx = oracle.new_caches_bf16(2, nb, w.guard)
+    oracle.store_mla_bf16(w.kv_latent, w.k_rope, w.index_k, w.slot_mapping, want16_main,
+                          want16_idx, nb)
+    for got, want in zip(main16 + idx16, want16_main + want16_idx):
+        assert np.array_equal(got.cpu().numpy(), want)
