@@ -164,9 +164,38 @@ def _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_c
             len(main_caches), nb, BLOCK_SIZE, cnt]
 
 
+def slot_report(slot_mapping, num_blocks: int) -> dict:
+    """Debug check of a slot_mapping, on the host (it copies the slots back and
+    synchronises, so it is not for the hot path): how many slots are written,
+    padded (-1), invalid (other out-of-range values) and duplicated among the
+    written ones.  Duplicates leave unspecified bytes in the caches."""
+    import numpy as np
+    s = slot_mapping.detach().to("cpu").numpy() if isinstance(slot_mapping, torch.Tensor) \
+        else np.asarray(slot_mapping)
+    s = s.astype(np.int64, copy=False)
+    cap = int(num_blocks) * BLOCK_SIZE
+    written = s[(s >= 0) & (s < cap)]
+    uniq = np.unique(written)
+    return {"written": int(written.size), "padded": int(np.count_nonzero(s == -1)),
+            "invalid": int(np.count_nonzero((s != -1) & ((s < 0) | (s >= cap)))),
+            "duplicates": int(written.size - uniq.size)}
+
+
+def _check_distinct(slot_mapping, main_caches, num_blocks, main_slot=MAIN_SLOT_BYTES):
+    nb = num_blocks if num_blocks is not None else \
+        main_caches[0].numel() // (BLOCK_SIZE * main_slot)
+    rep = slot_report(slot_mapping, nb)
+    if rep["duplicates"]:
+        raise ValueError(f"slot_mapping names {rep['duplicates']} slot(s) more than once")
+
+
 def store_mla_fp8(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
-                  num_blocks=None, invalid_count=None, stream=None) -> None:
-    """Fused direct publication of every token row into all replicas."""
+                  num_blocks=None, invalid_count=None, stream=None,
+                  check_slots: bool = False) -> None:
+    """Fused direct publication of every token row into all replicas.
+    check_slots=True first runs the host-side slot_report (debug only)."""
+    if check_slots:
+        _check_distinct(slot_mapping, main_caches, num_blocks)
     args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
                        num_blocks, invalid_count)
     check(lib().kvpub_store_mla_fp8(*args, _stream_handle(stream)))
