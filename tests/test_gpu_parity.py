@@ -293,3 +293,39 @@ def test_large_batch_matches_oracle(dev):
     w = inputs.prefill_batch(1000, 128, 1024, 8192)
     c = run_store(w, dev, "fused")
     assert_matches_oracle(c, *oracle_caches(w)[:2])
+
+
+def test_concurrent_host_threads_on_separate_streams(dev):
+    """Four host threads, each with its own CUDA stream and caches, publish
+    different batches at the same time; the library's cached launch geometry
+    and thread-local error state must not mix them up."""
+    import threading
+    ws = [inputs.random_rows(seed=700 + k, num_tokens=3000, num_blocks=60, num_replicas=2,
+                             pad_fraction=0.05) for k in range(4)]
+    xs = [DevInputs(w, dev) for w in ws]
+    cs = [Caches(2, w.num_blocks, w.guard, dev) for w in ws]
+    streams = [torch.cuda.Stream(device=dev) for _ in ws]
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(k):
+        try:
+            with torch.cuda.stream(streams[k]):
+                for _ in range(20):
+                    kvpub.store_mla_fp8(xs[k].lat, xs[k].rope, xs[k].idx, xs[k].slots,
+                                        cs[k].main, cs[k].idx)
+                    # a failing call on this thread must not disturb the others
+                    assert kvpub.lib().kvpub_epoch_advance(None, None) == 1
+                    assert "epoch" in kvpub.last_error()
+        except Exception as e:      # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for w, c in zip(ws, cs):
+        assert_matches_oracle(c, *oracle_caches(w)[:2])
