@@ -50,7 +50,9 @@
  *
  * Slots: slot_mapping[t] is an int64. -1 marks a padded token, which is
  * skipped. A value outside [0, num_blocks * 64) is invalid: it is skipped
- * too and counted. A skipped token's input row is not read. Slots must be
+ * too and counted. Nothing is written for a skipped token. Its input row may
+ * still be read, because some rows are loaded together with their slot, so
+ * every one of the num_tokens input rows must be readable. Slots must be
  * distinct. If two tokens name the same slot, the bytes left there are
  * unspecified.
  */

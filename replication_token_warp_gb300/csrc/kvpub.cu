@@ -183,16 +183,21 @@ __device__ __forceinline__ void copy_row_bf16(const StoreArgs &a, const RowRegs 
 
 // Grid-stride over token rows, one warp per row.  The next row's slot and
 // inputs are loaded before the current row is quantised, so each warp keeps
-// two rows of loads in flight.
+// two rows of loads in flight; the next row's inputs are read only if its
+// slot is written.
 template <int R, bool kFp8>
 __device__ __forceinline__ void publish_rows(const StoreArgs &a) {
     const int lane = threadIdx.x & 31;
     const int64_t num_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (t >= a.num_tokens) return;
-    int64_t s = a.slot_mapping[t];
+    // The warp's first row is loaded together with its slot instead of after
+    // it: one memory latency less at the start of every launch, which is most
+    // of a decode batch's time.  A padded row's inputs may be read this way
+    // (they exist: the caller passes num_tokens rows); nothing is written.
     RowRegs cur;
-    if (slot_written(s, a.num_slots)) load_row(a, t, lane, cur);
+    load_row(a, t, lane, cur);
+    int64_t s = a.slot_mapping[t];
     while (true) {
         const int64_t t_next = t + num_warps;
         int64_t s_next = -1;
