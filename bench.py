@@ -411,6 +411,26 @@ def e2e_measure(step: Step, steps: int, warmup: int):
     return ms, h2d, d2h, h2d_gbs
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo, else lscpu, else platform)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(budget_s: float):
     """The oracle as it stands, single-threaded, over as many layers of the
     same workload as fit in about budget_s seconds of oracle time (at least
@@ -430,7 +450,7 @@ def cpu_baseline(budget_s: float):
     return {"value": rows * R / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{layers} of {LAYERS} layers ({rows} rows x {R} replicas), "
                       f"scalar C oracle, 1 thread, {elapsed:.1f} s",
-            "host_cpus": os.cpu_count()}
+            "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_ours(args):
@@ -554,7 +574,7 @@ def run_reference(args):
            "config": {"workload": WORKLOAD, "layers": LAYERS, "rows_per_layer": ROWS,
                       "replicas": R, "blocks_per_replica": NUM_BLOCKS},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                            "sample": desc},
+                            "sample": desc, "host_cpus": os.cpu_count(), "cpu_model": cpu_model()},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)

@@ -249,6 +249,50 @@ def gather_insert_noalloc(kv_latent, k_rope, index_k, slot_mapping, main_caches,
     check(lib().kvpub_gather_insert_noalloc(*args, _stream_handle(stream)))
 
 
+class PreparedCall:
+    """One library call with its arguments marshalled once (shapes checked,
+    pointers and the replica pointer arrays built).  Calling it passes only
+    the stream, which cuts the per-call host cost of an eager (non-graph)
+    serving loop.  It keeps the tensors it was prepared with alive; they must
+    not be reallocated while it is in use."""
+
+    def __init__(self, fn, args, keep):
+        self._fn, self._args, self._keep = fn, tuple(args), keep
+
+    def __call__(self, stream=None) -> None:
+        check(self._fn(*self._args, _stream_handle(stream)))
+
+
+def prepare_store_mla_fp8(kv_latent, k_rope, index_k, slot_mapping, main_caches,
+                          indexer_caches, num_blocks=None, invalid_count=None) -> PreparedCall:
+    """store_mla_fp8 with its arguments marshalled once."""
+    args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                       num_blocks, invalid_count)
+    keep = (kv_latent, k_rope, index_k, slot_mapping, list(main_caches), list(indexer_caches),
+            invalid_count)
+    return PreparedCall(lib().kvpub_store_mla_fp8, args, keep)
+
+
+def prepare_store_mla_fp8_publish(kv_latent, k_rope, index_k, slot_mapping, main_caches,
+                                  indexer_caches, epoch, done_count, num_blocks=None,
+                                  invalid_count=None) -> PreparedCall:
+    """store_mla_fp8_publish with its arguments marshalled once."""
+    args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
+                       num_blocks, invalid_count)
+    _counter(epoch, (torch.int64, torch.uint64), "epoch")
+    _counter(done_count, (torch.int32, torch.uint32), "done_count")
+    keep = (kv_latent, k_rope, index_k, slot_mapping, list(main_caches), list(indexer_caches),
+            invalid_count, epoch, done_count)
+    return PreparedCall(lib().kvpub_store_mla_fp8_publish,
+                        args + [epoch.data_ptr(), done_count.data_ptr()], keep)
+
+
+def prepare_epoch_advance(epoch) -> PreparedCall:
+    """epoch_advance with its argument marshalled once."""
+    _counter(epoch, (torch.int64, torch.uint64), "epoch")
+    return PreparedCall(lib().kvpub_epoch_advance, [epoch.data_ptr()], (epoch,))
+
+
 def _counter(t, dtypes, name):
     if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in dtypes or t.numel() < 1:
         raise ValueError(f"{name}: expected a CUDA tensor of {dtypes}")

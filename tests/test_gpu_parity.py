@@ -329,3 +329,27 @@ def test_concurrent_host_threads_on_separate_streams(dev):
     assert not errors, errors
     for w, c in zip(ws, cs):
         assert_matches_oracle(c, *oracle_caches(w)[:2])
+
+
+def test_prepared_calls_match_the_plain_calls(dev):
+    """Calls prepared once (arguments marshalled up front) leave the same
+    bytes and advance the epoch the same way as the plain calls."""
+    w = inputs.make(2)
+    x = DevInputs(w, dev)
+    c = Caches(4, w.num_blocks, w.guard, dev)
+    c2 = Caches(4, w.num_blocks, w.guard, dev)
+    epoch = torch.zeros(1, dtype=torch.int64, device=dev)
+    done = torch.zeros(1, dtype=torch.int32, device=dev)
+    store = kvpub.prepare_store_mla_fp8(x.lat, x.rope, x.idx, x.slots, c.main, c.idx)
+    advance = kvpub.prepare_epoch_advance(epoch)
+    publish = kvpub.prepare_store_mla_fp8_publish(x.lat, x.rope, x.idx, x.slots, c2.main, c2.idx,
+                                                  epoch, done)
+    for _ in range(3):
+        store()
+        advance()
+        publish()
+    torch.cuda.synchronize()
+    assert int(epoch.item()) == 6 and int(done.item()) == 0
+    want = oracle_caches(w)[:2]
+    assert_matches_oracle(c, *want)
+    assert_matches_oracle(c2, *want)
