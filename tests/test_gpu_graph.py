@@ -9,6 +9,8 @@ replay).  After the replays, every layer's four replicas must equal the
 oracle byte for byte, red zones included.
 """
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -190,3 +192,17 @@ def test_every_capturable_call_replays_in_a_graph(dev):
                           want16_idx, nb)
     for got, want in zip(main16 + idx16, want16_main + want16_idx):
         assert np.array_equal(got.cpu().numpy(), want)
+
+
+def test_first_call_of_a_process_can_be_captured(cuda_device):
+    """A fresh process whose first kvpub call is inside graph capture."""
+    import json
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    kbuild.build()
+    res = subprocess.run([sys.executable, os.path.join(here, "capture_first_call.py")],
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    out = json.loads(res.stdout.strip().splitlines()[-1])
+    assert out == {"captured_first_call": True, "bytes_ok": True, "epoch": 1}, out
