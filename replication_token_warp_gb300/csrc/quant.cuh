@@ -8,21 +8,27 @@
 // reduction, and every lane quantises 20 values.
 //
 // Quantisation rule (the cache format's reading): per 128-element tile
-// amax = max |x|, scale = max(amax, 1e-4f) / 448 (one IEEE fp32 division),
+// amax = max |x|, scale = max(amax, 1e-4f) / 448 (correctly rounded fp32),
 // code = E4M3(x / scale) with round-to-nearest-even and saturation; a NaN in
 // the tile gives the scale 0x7FFFFFFF and codes 0x7F.
 //
 // The quotient x / scale must be the correctly rounded fp32 quotient.  It is
 // computed with Markstein's correction (P. Markstein, "Computation of
 // elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-// Dev. 34(1), 1990): with y = RN(1/scale) from one IEEE reciprocal per
-// tile, q0 = RN(x * y), r = x - scale * q0 (exact in one fma) and
-// q = RN(q0 + r * y) (one fma).  Per element that is one multiply and two
-// fmas, issued two elements at a time as packed f32x2 operations, then the
-// input's sign bit is ORed into each code (see quant4_markstein).  A tile
-// whose scale is not finite (an Inf or NaN in the tile) takes IEEE division.
-// Over every (x, amax) pair the kernel can meet, the codes this produces
-// equal those of IEEE division; a GPU test sweeps all of them.
+// Dev. 34(1), 1990): with y = RN(1/scale) per tile, q0 = RN(x * y),
+// r = x - scale * q0 (exact in one fma) and q = RN(q0 + r * y) (one fma).
+// Per element that is one multiply and two fmas, issued two elements at a
+// time as packed f32x2 operations, then the input's sign bit is ORed into
+// each code (see quant4_markstein).  A tile whose scale is not finite (an
+// Inf or NaN in the tile) takes IEEE division.
+//
+// The per-tile scale and reciprocal are themselves exact without an IEEE
+// division: the scale by the same correction with the constant RN(1/448)
+// (tile_scale), the reciprocal by one Newton-Raphson step from the hardware
+// approximation (tile_divisor).  Both are correctly rounded on every input
+// the kernel can meet: a tile maximum is one of 32,768 bf16 magnitudes, so
+// GPU tests compare them, and the codes of every (x, amax) pair, with
+// CUDA's __fdiv_rn and __frcp_rn.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -42,14 +48,21 @@ __device__ __forceinline__ uint32_t halves_max(uint32_t v) {
     return max(v & 0xffffu, v >> 16);
 }
 
-// max(amax, 1e-4f) / 448 in fp32.  The comparison is false for NaN, so a
-// NaN amax passes through and becomes the canonical quiet NaN.
+// RN(max(amax, 1e-4f) / 448) in fp32.  For a finite maximum, m is 1e-4f
+// or a bf16 magnitude above it, and Markstein's correction with the
+// constant c = RN(1/448) gives the correctly rounded quotient for every one
+// of those 18,095 values: q0 = RN(m c), r = m - 448 q0 (exact), RN(q0 + r c).
+// An Inf maximum gives Inf (as IEEE division would), a NaN maximum the
+// canonical quiet NaN.
 __device__ __forceinline__ float tile_scale(uint32_t amax_bits16) {
+    if (amax_bits16 >= 0x7f80u)
+        return __uint_as_float(amax_bits16 == 0x7f80u ? 0x7f800000u : 0x7fffffffu);
     const float amax = __uint_as_float(amax_bits16 << 16);
     const float m = (amax < 1e-4f) ? 1e-4f : amax;
-    float s = __fdiv_rn(m, 448.0f);
-    if (s != s) s = __uint_as_float(0x7fffffffu);
-    return s;
+    constexpr float c = 1.0f / 448.0f;
+    const float q0 = __fmul_rn(m, c);
+    const float r = __fmaf_rn(-448.0f, q0, m);
+    return __fmaf_rn(r, c, q0);
 }
 
 // Everything a lane needs to divide by one tile's scale.
@@ -60,11 +73,18 @@ struct TileDivisor {
     bool ieee;                    // scale is Inf or NaN: use IEEE division
 };
 
+// RN(1/scale) for the finite scales tile_scale returns (2.2e-7 .. 7.6e35,
+// all normal, as are their reciprocals): the hardware's approximate
+// reciprocal y0, then one Newton-Raphson step in fma form,
+// y = y0 + y0 (1 - scale y0).  Non-finite scales take IEEE division and do
+// not use y.
 __device__ __forceinline__ TileDivisor tile_divisor(float scale) {
     TileDivisor d;
     d.scale = scale;
     d.ieee = !(fabsf(scale) <= 3.402823466e38f);
-    const float y = __frcp_rn(scale);
+    float y0;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(scale));
+    const float y = __fmaf_rn(__fmaf_rn(-scale, y0, 1.0f), y0, y0);
     asm("mov.b64 %0, {%1, %1};" : "=l"(d.y2) : "f"(y));
     asm("mov.b64 %0, {%1, %1};" : "=l"(d.neg_s2) : "f"(-scale));
     return d;
