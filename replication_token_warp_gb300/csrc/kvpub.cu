@@ -82,9 +82,9 @@ __device__ __forceinline__ void st4(void *p, uint32_t v) {
 
 // Every kernel here is launched with programmatic stream serialization, so
 // its blocks may be scheduled while the previous kernel on the stream is
-// still finishing.  Each kernel's first instruction waits until that kernel
-// has completed and its memory is visible, so nothing is read or written
-// out of stream order; only the launch latency overlaps.
+// still finishing.  Each kernel waits, before it touches memory, until that
+// kernel has completed and its memory is visible, so nothing is read or
+// written out of stream order; only the launch latency overlaps.
 __device__ __forceinline__ void wait_previous_kernel() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -287,7 +287,17 @@ gather_rows_kernel(const StoreArgs a, uint8_t *workspace) {
     }
 }
 
+// The one-thread epoch kernel lets the next kernel on the stream be
+// scheduled at once (griddepcontrol.launch_dependents) instead of when it
+// exits.  The next kernel's blocks then become resident while this one is
+// still waiting for the store before it; their own wait still holds them
+// until this kernel has completed and its increment is visible.  In a graph
+// of store + epoch launches this takes the launch of the next store's grid
+// off the critical path (61-layer prefill step 0.756 -> 0.741 ms).  The
+// store kernels do not trigger early: there the next grid's blocks would
+// only compete with the running one for SM slots (measured slower).
 __global__ void epoch_advance_kernel(unsigned long long *epoch) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     wait_previous_kernel();
     release_add_epoch(epoch);
 }
