@@ -88,6 +88,15 @@ def test_padded_and_invalid_slots(dev):
     check(w, mf, xf)
 
 
+@pytest.mark.parametrize("delta", [-1, 0, 1])
+def test_batches_on_both_sides_of_the_block_size_switch(dev, delta):
+    # launches of fewer rows than SMs x 8 take 2-warp blocks, the rest 8-warp blocks
+    T = torch.cuda.get_device_properties(dev).multi_processor_count * 8 + delta
+    w = inputs.random_rows(seed=700 + delta, num_tokens=T, num_blocks=32, num_replicas=2,
+                           pad_fraction=0.05)
+    check(w, *run(w, dev))
+
+
 @pytest.mark.parametrize("R", [1, 3, 8])
 @pytest.mark.parametrize("T", [1, 33, 1000])
 def test_replicas_and_ragged_batches(dev, R, T):

@@ -4,8 +4,10 @@ replica's whole cache buffer plus 4 KiB red zones on both sides.
 Covers the five workloads, hand-derived rows (NaN, Inf, ties, saturation,
 subnormals), every bf16 value through the encoder at scale 1, scales from
 2^-40 to 2^40, strided input views, padded and invalid slots, 1..8
-replicas, ragged batch sizes, byte offsets beyond 2^31, the gather-then-
-insert path, the fused store+epoch launch, and the failure statuses.
+replicas (8 also on the capacity workload), ragged batch sizes, batches on
+both sides of the launch-shape switch (SMs x 8 rows), byte offsets beyond
+2^31, the gather-then-insert path, the fused store+epoch launch, and the
+failure statuses.
 Sources: "[Kernel][PCP] Publish replicated KV updates through PyTorch
 symmetric memory", Correctness and current-head validation (fp8_ds_mla,
 padded and invalid slots, guard bytes, byte-exact against gather-then-
@@ -155,6 +157,32 @@ def test_padded_and_invalid_slots(dev):
 def test_replica_counts_and_ragged_batches(dev, R, T):
     w = inputs.random_rows(seed=100 + R * 10 + T, num_tokens=T, num_blocks=16,
                            num_replicas=R, pad_fraction=0.1)
+    c = run_store(w, dev, "fused")
+    assert_matches_oracle(c, *oracle_caches(w)[:2])
+
+
+def _switch_rows(dev):
+    # launches of fewer rows than this take 2-warp blocks, the rest 8-warp blocks
+    return torch.cuda.get_device_properties(dev).multi_processor_count * 8
+
+
+@pytest.mark.parametrize("path", ["fused", "gather", "publish"])
+@pytest.mark.parametrize("delta", [-1, 0, 1])
+def test_batches_on_both_sides_of_the_block_size_switch(dev, path, delta):
+    T = _switch_rows(dev) + delta
+    w = inputs.random_rows(seed=300 + delta, num_tokens=T, num_blocks=32, num_replicas=3,
+                           pad_fraction=0.05)
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    c = run_store(w, dev, path, invalid_count=cnt)
+    assert_matches_oracle(c, *oracle_caches(w)[:2])
+    assert int(cnt.item()) == 0
+
+
+def test_capacity_workload_into_eight_replicas(dev):
+    """The capacity workload (706,624-slot caches, random slots) with the
+    maximum replica count instead of 4: 8 x 556 MB of caches, all byte-exact."""
+    w = inputs.make(4)
+    w.num_replicas = 8
     c = run_store(w, dev, "fused")
     assert_matches_oracle(c, *oracle_caches(w)[:2])
 
