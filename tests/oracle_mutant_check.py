@@ -5,8 +5,9 @@ Exit status 0 if every pin holds, 1 if one fails (a crash also counts as
 detection).  Used by test_oracle_mutants.py on deliberately broken copies
 of the oracle; the pins are the same facts as in test_oracle_*.py: the
 nearest-code brute force, the hand-derived rows, the pairs where a
-reciprocal multiply and a true division give different codes, and the
-slot-layout extents with padded and invalid slots.
+reciprocal multiply and a true division give different codes, the
+slot-layout extents with padded and invalid slots, gather-then-insert equal
+to direct publication, and the bf16 layout against numpy indexing.
 """
 
 import ctypes
@@ -39,6 +40,10 @@ def load(path):
                                       ctypes.POINTER(u8p), ctypes.POINTER(u8p), ctypes.c_int,
                                       ctypes.c_int64, i64p]
     lib.kvo_store_mla_fp8.restype = ctypes.c_int64
+    lib.kvo_gather_insert.argtypes = lib.kvo_store_mla_fp8.argtypes[:-1] + [u16p, i64p]
+    lib.kvo_gather_insert.restype = ctypes.c_int64
+    lib.kvo_store_mla_bf16.argtypes = lib.kvo_store_mla_fp8.argtypes
+    lib.kvo_store_mla_bf16.restype = ctypes.c_int64
     return lib
 
 
@@ -46,20 +51,29 @@ def ptr(a, t):
     return a.ctypes.data_as(ctypes.POINTER(t))
 
 
-def store(lib, lat, rope, idx, slots, R, nb, guard=0xA5):
-    main = [np.full(nb * 64 * 656, guard, np.uint8) for _ in range(R)]
-    ixc = [np.full(nb * 8448, guard, np.uint8) for _ in range(R)]
+def store(lib, lat, rope, idx, slots, R, nb, guard=0xA5, how="fp8"):
+    """One oracle call: how = "fp8" (direct), "gather" (gather-then-insert)
+    or "bf16" (the unquantised layout).  Returns (main, indexer, n, invalid)."""
+    main_bytes, idx_bytes = (nb * 64 * 1152, nb * 64 * 256) if how == "bf16" else \
+        (nb * 64 * 656, nb * 8448)
+    main = [np.full(main_bytes, guard, np.uint8) for _ in range(R)]
+    ixc = [np.full(idx_bytes, guard, np.uint8) for _ in range(R)]
     u8p = ctypes.POINTER(ctypes.c_uint8)
     mp = (u8p * R)(*[ptr(m, ctypes.c_uint8) for m in main])
     ip = (u8p * R)(*[ptr(x, ctypes.c_uint8) for x in ixc])
     lat, rope, idx = (np.ascontiguousarray(a) for a in (lat, rope, idx))
     slots = np.ascontiguousarray(slots, np.int64)
     inv = ctypes.c_int64()
-    n = lib.kvo_store_mla_fp8(ptr(lat, ctypes.c_uint16), lat.shape[1],
-                              ptr(rope, ctypes.c_uint16), rope.shape[1],
-                              ptr(idx, ctypes.c_uint16), idx.shape[1],
-                              ptr(slots, ctypes.c_int64), slots.shape[0], mp, ip, R, nb,
-                              ctypes.byref(inv))
+    args = [ptr(lat, ctypes.c_uint16), lat.shape[1], ptr(rope, ctypes.c_uint16), rope.shape[1],
+            ptr(idx, ctypes.c_uint16), idx.shape[1], ptr(slots, ctypes.c_int64), slots.shape[0],
+            mp, ip, R, nb]
+    if how == "gather":
+        ws = np.empty(max(1, slots.shape[0]) * 704, np.uint16)
+        n = lib.kvo_gather_insert(*args, ptr(ws, ctypes.c_uint16), ctypes.byref(inv))
+    elif how == "bf16":
+        n = lib.kvo_store_mla_bf16(*args, ctypes.byref(inv))
+    else:
+        n = lib.kvo_store_mla_fp8(*args, ctypes.byref(inv))
     return main, ixc, n, inv.value
 
 
@@ -153,9 +167,57 @@ def check_layout(lib):
             and np.array_equal(changed_i, ei))
 
 
+def _padded_workload():
+    w = inputs.make(1)                      # decode batch: 64 rows, 4 padded
+    slots = w.slot_mapping.copy()
+    cap = w.num_blocks * 64
+    slots[[3, 10]] = [cap + 7, -3]          # two invalid slots besides the padding
+    return w, slots
+
+
+def check_gather(lib):
+    """Gather-then-insert leaves the same bytes and counts as direct
+    publication, in every one of 3 replicas."""
+    w, slots = _padded_workload()
+    a = store(lib, w.kv_latent, w.k_rope, w.index_k, slots, 3, w.num_blocks)
+    b = store(lib, w.kv_latent, w.k_rope, w.index_k, slots, 3, w.num_blocks, how="gather")
+    if a[2:] != b[2:] or a[3] != 2:
+        return False
+    return all(np.array_equal(x, y) for x, y in zip(a[0] + a[1], b[0] + b[1]))
+
+
+def check_bf16(lib):
+    """bf16 layout: each written slot holds its row's little-endian bytes
+    (Main = latent | rope at s * 1152, Indexer = index_k at s * 256), in
+    every replica, and nothing else changes (two guard values)."""
+    w, slots = _padded_workload()
+    R, nb = 2, w.num_blocks
+    a_main, a_ix, n, inv = store(lib, w.kv_latent, w.k_rope, w.index_k, slots, R, nb, 0xA5, "bf16")
+    b_main, b_ix, _, _ = store(lib, w.kv_latent, w.k_rope, w.index_k, slots, R, nb, 0x5A, "bf16")
+    ok = [t for t, s in enumerate(slots.tolist()) if 0 <= s < nb * 64]
+    if n != len(ok) or inv != 2:
+        return False
+    want_main = np.full(nb * 64 * 1152, 0xA5, np.uint8).reshape(nb * 64, 1152)
+    want_ix = np.full(nb * 64 * 256, 0xA5, np.uint8).reshape(nb * 64, 256)
+    for t in ok:
+        s = slots[t]
+        want_main[s] = np.frombuffer(w.kv_latent[t].astype("<u2").tobytes() +
+                                     w.k_rope[t].astype("<u2").tobytes(), np.uint8)
+        want_ix[s] = np.frombuffer(w.index_k[t].astype("<u2").tobytes(), np.uint8)
+    for r in range(R):
+        if not (np.array_equal(a_main[r], want_main.ravel()) and
+                np.array_equal(a_ix[r], want_ix.ravel())):
+            return False
+        changed = (a_main[r] != 0xA5) | (b_main[r] != 0x5A)
+        if int(changed.sum()) != 1152 * len(ok):
+            return False
+    return True
+
+
 def main(path):
     lib = load(path)
-    for check in (check_encoder, check_hand_rows, check_true_division, check_layout):
+    for check in (check_encoder, check_hand_rows, check_true_division, check_layout,
+                  check_gather, check_bf16):
         if not check(lib):
             print(f"pin failed: {check.__name__}")
             return 1

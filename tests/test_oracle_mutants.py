@@ -8,7 +8,11 @@ Mistakes planted (all on the CPU, in the oracle only): a wrong scale divisor,
 a wrong floor, multiplying by a reciprocal, ties rounded up, truncation, a
 dropped sign, the subnormal spacing, the Main-row field order, interleaved
 Indexer rows, an Indexer-scale offset, an amax taken across tile borders,
-ignoring NaN, an off-by-one slot bound, and counting padding as invalid.
+ignoring NaN, an off-by-one slot bound, counting padding as invalid; in
+gather-then-insert a shifted workspace field, inserting into the first
+replica only and counting invalid slots once per replica; in the bf16
+layout a wrong Main or Indexer slot stride and the rope written over the
+latent.
 """
 
 import os
@@ -43,6 +47,17 @@ MUTANTS = {
                           "kvo_quantize_tile(latent + j * KVO_TILE, KVO_TILE + (j < 3 ? 1 : 0),"),
     "nan_ignored": ("if (has_nan) {", "if (0) {"),
     "slot_bound_off_by_one": ("return s >= 0 && s < num_slots;", "return s >= 0 && s <= num_slots;"),
+    "gather_workspace_rope_shifted": ("memcpy(w + KVO_LATENT_DIM, k_rope + t * rope_stride",
+                                      "memcpy(w + KVO_LATENT_DIM + 1, k_rope + t * rope_stride"),
+    "gather_first_replica_only": ("insert_row(&b, s, main_caches[r], indexer_caches[r]);",
+                                  "insert_row(&b, s, main_caches[0], indexer_caches[0]);"),
+    "gather_invalid_per_replica": ("if (r == 0 && s != -1) ++invalid;", "if (s != -1) ++invalid;"),
+    "bf16_main_stride": ("uint8_t *m = main_caches[r] + s * KVO_MAIN_SLOT_BF16;",
+                         "uint8_t *m = main_caches[r] + s * 1024;"),
+    "bf16_rope_before_latent": ("put_le16(m + 2 * KVO_LATENT_DIM + 2 * i, k_rope[t * rope_stride + i]);",
+                                "put_le16(m + 2 * i, k_rope[t * rope_stride + i]);"),
+    "bf16_indexer_stride": ("uint8_t *x = indexer_caches[r] + s * KVO_IDX_SLOT_BF16;",
+                            "uint8_t *x = indexer_caches[r] + s * 128;"),
     "padding_counted": ("if (s != -1) ++invalid;\n            continue;\n        }\n"
                         "        make_row_bytes(kv_latent",
                         "++invalid;\n            continue;\n        }\n        make_row_bytes(kv_latent"),
