@@ -25,8 +25,14 @@
  *    captured into a CUDA graph. Kernel parameters hold the pointers by
  *    value, so a replay reuses the same buffers.
  *  - Validation is fail-closed. Every check runs on the host before
- *    anything is enqueued. On any error nothing is launched, no byte
- *    changes, and kvpub_last_error() says why.
+ *    anything is enqueued. On any validation error nothing is launched, no
+ *    byte changes, and kvpub_last_error() says why.
+ *  - KVPUB_ERR_CUDA means the CUDA runtime refused a launch (or the device
+ *    query before it). A single-launch call then has enqueued nothing.
+ *    kvpub_gather_insert and kvpub_gather_insert_noalloc enqueue 1 + R
+ *    launches in turn and stop at the first refusal, so the launches before
+ *    it may already be on the stream. The stream is then in an error state
+ *    that the caller must handle anyway.
  *
  * Byte layout of one slot. The pages name the format (fp8_ds_mla Main-KV,
  * FP8 Indexer-K) but not its bytes. The reading used here is this:
