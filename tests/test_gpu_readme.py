@@ -1,7 +1,8 @@
-"""The Python example in README.md runs as written, and every slot it writes
-holds the bytes the CPU oracle computes from the example's own inputs (the
-example's caches start uninitialised, so only the written slots are
-compared; the whole-buffer checks are in test_gpu_parity.py)."""
+"""The repository's Python usage example (the first ```python block of the
+readme) runs as written, and every slot it writes holds the bytes the CPU
+oracle computes from the example's own inputs.  The example's caches start
+uninitialised, so only the written slots are compared; the whole-buffer
+checks are in test_gpu_parity.py."""
 
 import os
 import re
