@@ -6,6 +6,11 @@ pointers and the current torch stream, and raise ``KvpubError`` on a
 non-zero status.  There is no fallback: if the library is not built, the
 first call raises.
 
+The library launches on the calling thread's current CUDA device, so every
+tensor and stream passed here must live on that device; anything else is a
+``ValueError`` before a launch (run the call under
+``torch.cuda.device(tensor.device)``).
+
 Names follow the C ABI in include/kvpub.h: ``store_mla_fp8`` (fused direct
 publication into every replica), ``store_mla_bf16`` (the unquantised cache
 variant), ``store_mla_fp8_publish`` (the same store
@@ -101,10 +106,28 @@ def check(status: int) -> None:
         raise KvpubError(status, last_error())
 
 
-def _stream_handle(stream) -> int:
+def check_devices(devices, current: int) -> None:
+    """Raise ValueError unless every device in ``devices`` is CUDA device
+    ``current``.  The library launches on the calling thread's current
+    device and dereferences every pointer there, so a tensor (or stream) of
+    another GPU would make a kernel touch memory it cannot address."""
+    for d in devices:
+        if d.type != "cuda" or d.index != current:
+            raise ValueError(f"{d} is not the current CUDA device cuda:{current}: call "
+                             "under torch.cuda.device(...) of the tensors' device")
+
+
+def _current_device() -> int:
+    return torch.cuda.current_device()
+
+
+def _stream_handle(stream, current: int | None = None) -> int:
+    """The raw cudaStream_t to launch on: the current torch stream by
+    default.  A torch.cuda.Stream must belong to the current device."""
     if stream is None:
         stream = torch.cuda.current_stream()
     if isinstance(stream, torch.cuda.Stream):
+        check_devices([stream.device], _current_device() if current is None else current)
         return stream.cuda_stream
     return int(stream)
 
@@ -160,6 +183,10 @@ def _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_c
         if invalid_count.dtype not in (torch.int64, torch.uint64) or not invalid_count.is_cuda:
             raise ValueError("invalid_count: expected an int64 CUDA tensor")
         cnt = invalid_count.data_ptr()
+    tensors = [kv_latent, k_rope, index_k, slot_mapping, *main_caches, *indexer_caches]
+    if invalid_count is not None:
+        tensors.append(invalid_count)
+    check_devices([t.device for t in tensors], _current_device())
     return [lp, ls, rp, rs, ip, is_, slot_mapping.data_ptr(), T, mains, idxs,
             len(main_caches), nb, BLOCK_SIZE, cnt]
 
@@ -233,6 +260,7 @@ def gather_insert(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer
                        num_blocks, invalid_count)
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace: expected a contiguous CUDA tensor")
+    check_devices([workspace.device], _current_device())
     nbytes = workspace.numel() * workspace.element_size()
     check(lib().kvpub_gather_insert(*args, workspace.data_ptr(), nbytes,
                                     _stream_handle(stream)))
@@ -258,9 +286,12 @@ class PreparedCall:
 
     def __init__(self, fn, args, keep):
         self._fn, self._args, self._keep = fn, tuple(args), keep
+        self._device = _current_device()
 
     def __call__(self, stream=None) -> None:
-        check(self._fn(*self._args, _stream_handle(stream)))
+        current = _current_device()
+        check_devices([torch.device("cuda", self._device)], current)
+        check(self._fn(*self._args, _stream_handle(stream, current)))
 
 
 def prepare_store_mla_fp8(kv_latent, k_rope, index_k, slot_mapping, main_caches,
@@ -296,6 +327,7 @@ def prepare_epoch_advance(epoch) -> PreparedCall:
 def _counter(t, dtypes, name):
     if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in dtypes or t.numel() < 1:
         raise ValueError(f"{name}: expected a CUDA tensor of {dtypes}")
+    check_devices([t.device], _current_device())
 
 
 def epoch_advance(epoch: torch.Tensor, stream=None) -> None:
