@@ -236,9 +236,11 @@ kvpub_status kvpub_gather_insert(
  *
  *  - num_tokens above KVPUB_STATIC_GATHER_MAX_TOKENS gives
  *    KVPUB_ERR_WORKSPACE, and nothing is launched.
- *  - The first call on each device looks up the array's device address with
- *    that device current, and keeps it for later calls. Make that first call
- *    before any stream capture on the device.
+ *  - Every call looks up the array's device address for the current device
+ *    (a host-side lookup; nothing is cached, so the call stays valid after a
+ *    cudaDeviceReset, which reloads the array at another address). The
+ *    first call on a device may load the library's device code there: make
+ *    it before any stream capture on that device.
  *  - Every call uses the same array. Calls that can overlap on the GPU (on
  *    different streams, or issued from several threads without ordering)
  *    race on it and corrupt each other's rows. Issue them on one stream.

@@ -715,8 +715,10 @@ extern "C" const char *kvpub_last_error(void) { return g_last_error; }
 // memory.  Every GPU that loads the library holds the array
 // (KVPUB_STATIC_GATHER_MAX_TOKENS rows of 1408 bytes, 5.5 MiB) until the
 // process exits.  Host code cannot use the array's name as a device address:
-// the first call on each device looks the address up with that device
-// current and caches it.
+// every call looks the address up for the current device.  The address is
+// not cached, because it belongs to the device's context: after a
+// cudaDeviceReset the array is reloaded at another address, and a cached
+// one would point at freed memory.
 
 static __device__ __align__(256) uint8_t
     g_static_gather_workspace[KVPUB_STATIC_GATHER_MAX_TOKENS * KVPUB_GATHER_ROW_BYTES];
@@ -724,23 +726,16 @@ static __device__ __align__(256) uint8_t
 namespace kvpub {
 namespace {
 
-std::atomic<uint8_t *> g_static_workspace_addr[kMaxDevices];
-
 kvpub_status static_gather_workspace(uint8_t **out) {
     int dev = 0;
     kvpub_status st = current_device(&dev);
     if (st != KVPUB_OK) return st;
-    uint8_t *p = g_static_workspace_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        void *addr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&addr, g_static_gather_workspace);
-        if (e != cudaSuccess || addr == nullptr)
-            return fail(KVPUB_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s",
-                        cudaGetErrorString(e));
-        p = static_cast<uint8_t *>(addr);
-        g_static_workspace_addr[dev].store(p, std::memory_order_release);
-    }
-    *out = p;
+    void *addr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&addr, g_static_gather_workspace);
+    if (e != cudaSuccess || addr == nullptr)
+        return fail(KVPUB_ERR_CUDA, "cudaGetSymbolAddress(static workspace) on device %d: %s",
+                    dev, cudaGetErrorString(e));
+    *out = static_cast<uint8_t *>(addr);
     return KVPUB_OK;
 }
 

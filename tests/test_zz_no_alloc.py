@@ -9,9 +9,10 @@ library.
 
 This file calls that entry point through the C ABI twice in a row, each
 time with different rows and a different replica count. Both calls must
-leave the same bytes as kvpub_gather_insert with a caller-owned workspace:
-byte for byte, the tolerance of every cache test here. A batch above the
-fixed limit must be refused with nothing launched.
+leave the same bytes as kvpub_gather_insert with a caller-owned workspace,
+and the same bytes as the CPU oracle computes from the same inputs: byte for
+byte over whole buffers and red zones, the tolerance of every cache test
+here. A batch above the fixed limit must be refused with nothing launched.
 
 The file sits last in collection order, so a run that stops at its first
 failure has already run every other test.
@@ -22,7 +23,7 @@ import ctypes
 import pytest
 import torch
 
-from gpu_util import Caches, DevInputs
+from gpu_util import Caches, DevInputs, assert_matches_oracle, oracle_caches
 from replication_token_warp_gb300 import build as kbuild
 from replication_token_warp_gb300 import inputs, kvpub
 
@@ -70,6 +71,9 @@ def test_noalloc_matches_gather_insert_twice(dev):
         for a, b in zip(want.main_full + want.idx_full, got.main_full + got.idx_full):
             assert torch.equal(a, b)
         assert int(n_got.item()) == int(n_want.item())
+        want_main, want_idx, _, n_invalid = oracle_caches(w)
+        assert_matches_oracle(got, want_main, want_idx)
+        assert int(n_got.item()) == n_invalid
         written = sum(int((b != w.guard).sum().item()) for b in got.main)
         assert written > 0.9 * 656 * w.num_valid * w.num_replicas
 
