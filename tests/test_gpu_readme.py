@@ -1,11 +1,11 @@
-"""The repository's Python usage example (the first ```python block of the
-readme) runs as written, and every slot it writes holds the bytes the CPU
-oracle computes from the example's own inputs.  The example's caches start
-uninitialised, so only the written slots are compared; the whole-buffer
-checks are in test_gpu_parity.py."""
+"""The repository's Python usage example (tests/readme_example.py, shown in
+the readme) runs as written, and every slot it writes holds the bytes the
+CPU oracle computes from the example's own inputs.  The example's caches
+start uninitialised, so only the written slots are compared; the
+whole-buffer checks are in test_gpu_parity.py."""
 
 import os
-import re
+import runpy
 
 import numpy as np
 import pytest
@@ -17,22 +17,13 @@ from replication_token_warp_gb300 import kvpub
 
 pytestmark = pytest.mark.gpu
 
-README = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "README.md")
-
-
-def _example() -> str:
-    with open(README) as f:
-        text = f.read()
-    m = re.search(r"```python\n(.*?)```", text, re.S)
-    assert m, "README.md has no python example"
-    return m.group(1)
+EXAMPLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "readme_example.py")
 
 
 def test_readme_example_matches_the_oracle(cuda_device):
     kbuild.build()
     kvpub.lib()
-    ns = {}
-    exec(_example(), ns)
+    ns = runpy.run_path(EXAMPLE)
     torch.cuda.synchronize()
     assert int(ns["epoch"].item()) == 1
 
