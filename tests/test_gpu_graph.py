@@ -115,6 +115,67 @@ def test_separate_epoch_lanes_in_one_graph(dev):
         assert lanes.tolist() == [7 * k, 4 * k]
 
 
+def test_two_dbo_lanes_on_two_streams_in_one_graph(dev):
+    """Two micro-batch lanes, as in dual-batch overlap: each lane stores its
+    own layers' rows into its own caches and advances its own epoch after
+    every layer, on its own stream forked from the capture stream.  The
+    launches are issued interleaved, and lane B's store of layer k also
+    waits for lane A's epoch advance of layer k (an event across streams).
+    On every one of 10 replays both counters must be exact, and afterwards
+    both lanes' caches must equal the oracle's bytes ("[Kernel][PCP] Publish
+    replicated KV updates through PyTorch symmetric memory", Design: the
+    device-epoch barrier supports CUDA Graph replay and separate DBO
+    lanes)."""
+    from gpu_util import DevInputs
+    layers = {"A": 4, "B": 3}
+    R, nb = 2, 96
+    ws = {lane: [inputs.prefill_batch(600 + 10 * i + layer, 2, 1024, nb, R)
+                 for layer in range(n)] for i, (lane, n) in enumerate(layers.items())}
+    xs = {lane: [DevInputs(w, dev) for w in ws[lane]] for lane in layers}
+    caches = {lane: [Caches(R, nb, inputs.GUARD_BYTE, dev) for _ in ws[lane]] for lane in layers}
+    epochs = torch.zeros(2, dtype=torch.int64, device=dev)
+    epoch = {"A": epochs[0:1], "B": epochs[1:2]}
+
+    def store(lane, layer):
+        x, c = xs[lane][layer], caches[lane][layer]
+        kvpub.store_mla_fp8(x.lat, x.rope, x.idx, x.slots, c.main, c.idx, nb)
+        kvpub.epoch_advance(epoch[lane])
+
+    for lane in layers:                        # load the kernels before capture
+        store(lane, 0)
+    torch.cuda.synchronize()
+    epochs.zero_()
+
+    lane_a, lane_b = torch.cuda.Stream(), torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        main = torch.cuda.current_stream()
+        lane_a.wait_stream(main)
+        lane_b.wait_stream(main)
+        for layer in range(max(layers.values())):
+            done_a = torch.cuda.Event()
+            if layer < layers["A"]:
+                with torch.cuda.stream(lane_a):
+                    store("A", layer)
+                    done_a.record(lane_a)
+            if layer < layers["B"]:
+                with torch.cuda.stream(lane_b):
+                    if layer < layers["A"]:
+                        lane_b.wait_event(done_a)
+                    store("B", layer)
+        main.wait_stream(lane_a)
+        main.wait_stream(lane_b)
+    torch.cuda.synchronize()
+    assert epochs.tolist() == [0, 0]           # capture runs nothing
+    for k in range(1, REPLAYS + 1):
+        g.replay()
+        torch.cuda.synchronize()
+        assert epochs.tolist() == [layers["A"] * k, layers["B"] * k]
+    for lane in layers:
+        for w, c in zip(ws[lane], caches[lane]):
+            assert_matches_oracle(c, *oracle_caches(w)[:2])
+
+
 def test_bench_step_matches_oracle(dev):
     """The benchmark's own launch configuration: packed [T, 704] rows passed
     as strided views, one graph of 61 x (store + epoch advance), and the
