@@ -10,10 +10,29 @@ concurrency 4, GLM-5.2's sparse layers) with seeded synthetic bf16 rows.
 
 Prints one JSON line: rows stored per second x replicas (whole job), the
 roofline of the store kernel against the measured HBM copy bandwidth, the
-end-to-end figure through the public API with host inputs, and the CPU
-oracle timed on the host as a baseline.
+end-to-end figure through the public API with host inputs, the CPU oracle
+timed on the host as a baseline, and under "workloads" the store kernel's
+roofline fraction on each bandwidth-bound workload: the c16 x 1,024 prefill,
+this c4 x 3,584 prefill and the 706,624-slot capacity batch.  Before any
+timing, the timed buffers are compared byte for byte with the oracle's.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 outside torchrun, the script starts itself again under
+torch.distributed.run with N local ranks (one per GPU).
+
+The DRAM traffic in the roofline comes from profiles/store_mla_fp8_prefill_
+c4x3584.json, which ``--write-traffic`` writes from the CSV of this ncu
+capture (a 3-layer run of the same launches; 3 captured store launches):
+
+  python bench.py --layers 3 --steps 1 --warmup 3 --no-cpu-baseline --no-e2e \
+      --no-workloads
+  ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --print-units base \
+      --cache-control none --clock-control none -k regex:store_mla_fp8_kernel \
+      -s 14 -c 3 --csv --log-file dram_prefill.csv \
+      python bench.py --layers 3 --steps 1 --warmup 3 --no-cpu-baseline --no-e2e \
+      --no-workloads
+  python bench.py --write-traffic dram_prefill.csv
 """
 
 from __future__ import annotations
@@ -22,7 +41,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -49,7 +67,17 @@ NUM_BLOCKS = 1024
 ROW_IN = 1408                  # bf16 bytes read per valid row
 ROW_OUT = 656 + 132            # bytes written per valid row and replica
 FALLBACK_HBM_GBS = 6800.0
-PROFILE = os.path.join(ROOT, "profiles", "store_mla_fp8_prefill_c4x3584.md")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "store_mla_fp8_prefill_c4x3584.json")
+TRAFFIC_LAYERS = 3
+# store_mla_fp8_kernel launches before the first timed replay of a
+# --layers 3 --no-cpu-baseline run: the direct-vs-gather check (1 + 4),
+# two eager passes before the captures (3 + 3) and one replay (3).
+TRAFFIC_SKIP = 5 + 3 * TRAFFIC_LAYERS
+TRAFFIC_RUN = (f"python bench.py --layers {TRAFFIC_LAYERS} --steps 1 --warmup 3 "
+               "--no-cpu-baseline --no-e2e --no-workloads")
+TRAFFIC_CMD = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --print-units base "
+               "--cache-control none --clock-control none -k regex:store_mla_fp8_kernel "
+               f"-s {TRAFFIC_SKIP} -c {TRAFFIC_LAYERS} --csv --log-file <csv> {TRAFFIC_RUN}")
 
 
 def gather_insert_bytes(num_tokens: int, num_valid: int, replicas: int) -> int:
@@ -95,17 +123,68 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the kernel source as it stands (else None)."""
+    """Per-launch DRAM bytes of the headline store kernel from the committed
+    ncu summary, if it was captured on the kernel source as it stands (else
+    None)."""
     try:
-        text = open(PROFILE).read()
-    except OSError:
+        with open(TRAFFIC_JSON) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    return int(m_bytes.group(1))
+    return int(rec["dram_bytes_per_launch"])
+
+
+_UNIT_SCALE = {"byte": 1, "kbyte": 10**3, "mbyte": 10**6, "gbyte": 10**9,
+               "kibyte": 2**10, "mibyte": 2**20, "gibyte": 2**30}
+
+
+def read_ncu_csv(path: str, kernel: str = "store_mla_fp8_kernel"):
+    """{launch id: {metric: bytes}} for the launches of ``kernel`` in an ncu
+    --csv --metrics log (the log's own banner lines are skipped)."""
+    import csv
+    with open(path, newline="") as f:
+        lines = f.read().splitlines()
+    start = next(i for i, l in enumerate(lines) if l.startswith('"ID"'))
+    launches = {}
+    for row in csv.DictReader(lines[start:]):
+        if kernel not in row["Kernel Name"]:
+            continue
+        unit = row.get("Metric Unit", "byte").strip().lower() or "byte"
+        value = float(row["Metric Value"].replace(",", "")) * _UNIT_SCALE.get(unit, 1)
+        launches.setdefault(int(row["ID"]), {})[row["Metric Name"]] = value
+    return launches
+
+
+def write_traffic(csv_path: str) -> dict:
+    """Turn the ncu capture named in the module docstring into the traffic
+    record that the roofline reads, stamped with the current source hash."""
+    launches = read_ncu_csv(csv_path)
+    if not launches:
+        raise SystemExit(f"no store_mla_fp8_kernel launches in {csv_path}")
+    reads = [m["dram__bytes_read.sum"] for m in launches.values()]
+    writes = [m["dram__bytes_write.sum"] for m in launches.values()]
+    slots = inputs.layer_slot_mapping()
+    rec = {
+        "kernel": f"store_mla_fp8_kernel<{R}>",
+        "workload": f"prefill_c4x3584 ({TRAFFIC_LAYERS} of {LAYERS} layers: the same "
+                    f"{ROWS}-row, {R}-replica launches as the timed graph)",
+        "kernel_source_sha256_16": kernel_source_hash(),
+        "launches": len(launches),
+        "dram_bytes_read_per_launch": int(round(statistics.mean(reads))),
+        "dram_bytes_write_per_launch": int(round(statistics.mean(writes))),
+        "dram_bytes_per_launch": int(round(statistics.mean(reads) + statistics.mean(writes))),
+        "algorithmic_bytes_per_launch": store_bytes(ROWS, int(np.count_nonzero(slots >= 0)), R),
+        "per_launch": [{"read": int(m["dram__bytes_read.sum"]),
+                        "write": int(m["dram__bytes_write.sum"])}
+                       for _, m in sorted(launches.items())],
+        "command": TRAFFIC_CMD,
+    }
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 class ClockSampler:
@@ -431,26 +510,90 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def cpu_baseline(budget_s: float):
-    """The oracle as it stands, single-threaded, over as many layers of the
-    same workload as fit in about budget_s seconds of oracle time (at least
-    one layer); input generation is outside the timed calls."""
-    import oracle
-    slots = inputs.layer_slot_mapping()
-    main, idx = oracle.new_caches(R, NUM_BLOCKS)
-    rows, layers, elapsed = 0, 0, 0.0
-    while layers < LAYERS and (layers == 0 or elapsed < budget_s):
-        w = inputs.prefill_layer(layers, slots)
+class OracleLeg:
+    """The CPU-baseline leg: the oracle as it stands (one thread) on a
+    bounded sample of the benchmark's own inputs.  The bytes it computes are
+    also compared with the GPU's timed buffers before any timing ("byte-
+    exact against gather-then-insert oracles before timing", as on
+    "[Kernel][PCP] Publish replicated KV updates through PyTorch symmetric
+    memory", Correctness and current-head validation).  Rank 0 of a
+    single-rank run only."""
+
+    def __init__(self):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.elapsed = 0.0          # oracle seconds on the headline workload
+        self.row_replicas = 0
+        self.layers = []
+        self.checked = {}
+
+    def _store(self, w, replicas, num_blocks):
+        main, idx = self.oracle.new_caches(replicas, num_blocks, inputs.GUARD_BYTE)
         t = time.perf_counter()
-        n, _ = oracle.store_mla_fp8(w.kv_latent, w.k_rope, w.index_k, w.slot_mapping, main, idx,
-                                    NUM_BLOCKS)
-        elapsed += time.perf_counter() - t
-        rows += n
-        layers += 1
-    return {"value": rows * R / elapsed, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{layers} of {LAYERS} layers ({rows} rows x {R} replicas), "
-                      f"scalar C oracle, 1 thread, {elapsed:.1f} s",
-            "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
+        n, _ = self.oracle.store_mla_fp8(w.kv_latent, w.k_rope, w.index_k, w.slot_mapping,
+                                         main, idx, num_blocks)
+        return main, idx, n, time.perf_counter() - t
+
+    def check(self, name: str, w, gpu_main, gpu_idx, replicas: int, num_blocks: int,
+              headline_layer: int | None = None):
+        """Compare one launch's GPU caches (every replica's whole buffer) with
+        the oracle's bytes; raise on any difference."""
+        main, idx, n, dt = self._store(w, replicas, num_blocks)
+        if headline_layer is not None:
+            self.elapsed += dt
+            self.row_replicas += n * replicas
+            self.layers.append(headline_layer)
+        for r in range(replicas):
+            for got, want, what in ((gpu_main[r], main[r], "Main"), (gpu_idx[r], idx[r], "Indexer")):
+                if not np.array_equal(got.cpu().numpy(), want):
+                    raise RuntimeError(f"{name}: {what} cache of replica {r} differs from "
+                                       "the oracle")
+        self.checked[name] = f"{replicas} replicas x (Main + Indexer), whole buffers"
+
+    def fill(self, budget_s: float):
+        """More headline layers, timed, until about budget_s oracle seconds."""
+        slots = inputs.layer_slot_mapping()
+        layer = 1
+        while self.elapsed < budget_s and layer < LAYERS:
+            if layer not in self.layers:
+                _, _, n, dt = self._store(inputs.prefill_layer(layer, slots), R, NUM_BLOCKS)
+                self.elapsed += dt
+                self.row_replicas += n * R
+                self.layers.append(layer)
+            layer += 1
+
+    def baseline(self):
+        return {"value": self.row_replicas / self.elapsed, "unit": UNIT, "cores": 1,
+                "kind": "oracle",
+                "sample": f"{len(self.layers)} of {LAYERS} layers of {WORKLOAD} "
+                          f"({self.row_replicas // R} rows x {R} replicas), scalar C oracle, "
+                          f"1 thread, {self.elapsed:.1f} s",
+                "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
+
+
+def roofline_entry(spec: Spec, step: Step, store_ms: float, steps: int, peak: float,
+                   clocks: dict, checked: bool):
+    """One workload's store-kernel figures: mean launch time from a graph of
+    all its store launches, algorithmic bytes per launch, GB/s, fraction of
+    the measured copy peak."""
+    L = spec.layers
+    per_launch = sum(store_bytes(step.num_tokens, v, spec.replicas, spec.bf16_cache)
+                     for v in step.valid) / L
+    kernel_ms = store_ms / (steps * L)
+    achieved = per_launch / (kernel_ms / 1e3) / 1e9
+    return {"kernel": f"store_mla_{'bf16' if spec.bf16_cache else 'fp8'}_kernel<{spec.replicas}>",
+            "rows_per_launch": step.num_tokens, "valid_rows_per_launch": step.valid[0],
+            "replicas": spec.replicas, "blocks_per_replica": spec.num_blocks,
+            "launches_per_step": L, "kernel_us": round(kernel_ms * 1e3, 3),
+            "algorithmic_bytes": int(round(per_launch)), "achieved": round(achieved, 1),
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "clocks": clocks,
+            "oracle_checked_before_timing": checked, "note": spec.note}
+
+
+# the bandwidth-bound workloads timed after the headline, each one
+# launch per buffer copy, copies distinct so a step exceeds L2
+SIDE_WORKLOADS = ("prefill_c16x1024", "capacity_706624")
 
 
 def run_ours(args):
@@ -460,81 +603,144 @@ def run_ours(args):
     kbuild.build()
     kvpub.lib()
     spec = SPECS[args.workload]()
+    if args.layers is not None:
+        if not 1 <= args.layers <= spec.layers:
+            raise SystemExit(f"--layers must be in 1..{spec.layers}")
+        spec.layers = args.layers
+        spec.note += f" (first {args.layers} layers only)"
     if args.path == "gather" and spec.bf16_cache:
         raise SystemExit("the gather-then-insert path exists for the fp8 cache only")
+    leg = OracleLeg() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     step = Step(dev, spec, args.path)
     L, Rr = spec.layers, spec.replicas
     checked = check_direct_equals_gather(step)
     g = step.capture(with_epoch=True)
     g_store = step.capture(with_epoch=False)
-    with ClockSampler(local) as clocks:
-        total_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
-        store_ms, _, _ = time_graph(g_store, args.steps, args.warmup)
-    total_ms = max_over_ranks(total_ms)
-    ms_per_step = total_ms / args.steps
-    expected_epoch = L * (args.warmup + args.steps)
-    epoch = int(step.epoch.item())
-    if epoch != expected_epoch:
-        raise RuntimeError(f"epoch {epoch} != {expected_epoch}: launches were lost")
-
-    rows_x_r = sum(step.valid) * Rr
-    value = whole_job_rate(world, rows_x_r, ms_per_step)
-    if args.path == "gather":
-        launch_bytes = [gather_insert_bytes(step.num_tokens, v, Rr) for v in step.valid]
-        kernel_name = f"gather_rows_kernel + {Rr} x store_mla_fp8_kernel<1> (per layer)"
-    else:
-        launch_bytes = [store_bytes(step.num_tokens, v, Rr, spec.bf16_cache) for v in step.valid]
-        kernel_name = f"store_mla_{'bf16' if spec.bf16_cache else 'fp8'}_kernel<{Rr}>"
-    per_launch = sum(launch_bytes) / L
+    # one replay fills the timed buffers; the oracle checks them before timing
+    g.replay()
+    torch.cuda.synchronize()
+    oracle_checked = False
+    if leg is not None and spec.name == WORKLOAD and args.path == "direct":
+        for layer in sorted({0, L - 1}):
+            w = spec.make(layer)
+            leg.check(f"{WORKLOAD}[{layer}]", w, step.main[layer], step.idx[layer], Rr,
+                      spec.num_blocks, headline_layer=layer)
+        oracle_checked = True
     peak, peak_kind = measured_peak()
-    kernel_ms = store_ms / (args.steps * L)
-    timing = (f"CUDA events around {args.steps} replays of a graph of the same {L} layers' "
-              f"store launches (no epoch kernels) / {args.steps * L} layers, gaps included")
-    achieved = per_launch / (kernel_ms / 1e3) / 1e9
-    traffic = profiled_traffic() if (spec.name == WORKLOAD and args.path == "direct") else None
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": kernel_name,
-                "algorithmic_bytes": int(round(per_launch)),
-                "kernel_us": round(kernel_ms * 1e3, 2), "peak_source": f"{peak_kind} hbm_gbs",
-                "timing": timing}
+    with ClockSampler(local) as sampler:
+        total_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
+        store_ms, s0, s1 = time_graph(g_store, args.steps, args.warmup)
+        clocks = sampler.summary(t0, t1)
+        store_clocks = sampler.summary(s0, s1)
+        total_ms = max_over_ranks(total_ms)
+        store_ms = max_over_ranks(store_ms)
+        ms_per_step = total_ms / args.steps
+        expected_epoch = L * (1 + args.warmup + args.steps)
+        epoch = int(step.epoch.item())
+        if epoch != expected_epoch:
+            raise RuntimeError(f"epoch {epoch} != {expected_epoch}: launches were lost")
 
-    e2e = None
-    if not args.no_e2e:
-        e2e_steps = max(3, min(args.steps, 50))
-        e2e_ms, h2d, d2h, h2d_gbs = e2e_measure(step, e2e_steps, max(1, min(args.warmup, 3)))
-        e2e_ms = max_over_ranks(e2e_ms)
-        floor_ms = h2d / (h2d_gbs * 1e6)
-        e2e = {"value": whole_job_rate(world, rows_x_r, e2e_ms / e2e_steps), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
-               "h2d_gbs_measured": round(h2d_gbs, 1),
-               "transfer_floor_ms": round(floor_ms, 4),
-               "frac_of_transfer_floor": round(floor_ms / (e2e_ms / e2e_steps), 4)}
+        rows_x_r = sum(step.valid) * Rr
+        value = whole_job_rate(world, rows_x_r, ms_per_step)
+        if args.path == "gather":
+            launch_bytes = [gather_insert_bytes(step.num_tokens, v, Rr) for v in step.valid]
+            kernel_name = f"gather_rows_kernel + {Rr} x store_mla_fp8_kernel<1> (per layer)"
+        else:
+            launch_bytes = [store_bytes(step.num_tokens, v, Rr, spec.bf16_cache)
+                            for v in step.valid]
+            kernel_name = f"store_mla_{'bf16' if spec.bf16_cache else 'fp8'}_kernel<{Rr}>"
+        per_launch = sum(launch_bytes) / L
+        kernel_ms = store_ms / (args.steps * L)
+        timing = (f"CUDA events around {args.steps} replays of a graph of the same {L} layers' "
+                  f"store launches (no epoch kernels) / {args.steps * L} layers, gaps included")
+        achieved = per_launch / (kernel_ms / 1e3) / 1e9
+        traffic = (profiled_traffic() if (spec.name == WORKLOAD and args.path == "direct")
+                   else None)
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "kernel": kernel_name, "algorithmic_bytes": int(round(per_launch)),
+                    "kernel_us": round(kernel_ms * 1e3, 2),
+                    "peak_source": f"{peak_kind} hbm_gbs", "timing": timing,
+                    "traffic_source": (f"{os.path.relpath(TRAFFIC_JSON, ROOT)} (ncu, "
+                                       f"{TRAFFIC_LAYERS}-layer run of the same launches)"
+                                       if traffic is not None else None)}
+
+        e2e = None
+        if not args.no_e2e:
+            e2e_steps = max(3, min(args.steps, 50))
+            e2e_ms, h2d, d2h, h2d_gbs = e2e_measure(step, e2e_steps,
+                                                    max(1, min(args.warmup, 3)))
+            e2e_ms = max_over_ranks(e2e_ms)
+            floor_ms = h2d / (h2d_gbs * 1e6)
+            e2e = {"value": whole_job_rate(world, rows_x_r, e2e_ms / e2e_steps), "unit": UNIT,
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
+                   "h2d_gbs_measured": round(h2d_gbs, 1),
+                   "transfer_floor_ms": round(floor_ms, 4),
+                   "frac_of_transfer_floor": round(floor_ms / (e2e_ms / e2e_steps), 4)}
+
+        workloads = {}
+        if spec.name == WORKLOAD and args.path == "direct" and not spec.bf16_cache:
+            workloads[WORKLOAD] = roofline_entry(spec, step, store_ms, args.steps, peak,
+                                                 store_clocks, oracle_checked)
+        launches_per_step = step.launches_per_layer() * L
+        l2_note = ("inputs larger than L2: one step touches "
+                   f"{sum(launch_bytes) / 1e9:.2f} GB")
+        del g, g_store, step
+        torch.cuda.empty_cache()
+        if not args.no_workloads and spec.name == WORKLOAD and args.path == "direct":
+            for name in SIDE_WORKLOADS:
+                workloads[name] = time_side_workload(dev, name, args, peak, sampler, leg)
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": spec.name, "layers": L, "rows_per_layer": step.num_tokens,
-                   "valid_rows_per_layer": step.valid[0], "replicas": Rr,
-                   "blocks_per_replica": spec.num_blocks,
-                   "launches_per_step": step.launches_per_layer() * L, "path": args.path,
+        "config": {"workload": spec.name, "layers": L, "rows_per_layer": ROWS
+                   if spec.name == WORKLOAD else None,
+                   "replicas": Rr, "blocks_per_replica": spec.num_blocks,
+                   "launches_per_step": launches_per_step, "path": args.path,
                    "graph": True, "parallelism": f"replicas only x{world}", "note": spec.note,
                    "direct_equals_gather_before_timing": checked,
-                   "l2": "inputs larger than L2: one step touches "
-                         f"{sum(launch_bytes) / 1e9:.2f} GB",
+                   "oracle_checked_before_timing": oracle_checked,
+                   "l2": l2_note,
                    "hbm_gbs_step": round(sum(launch_bytes) / (ms_per_step / 1e3) / 1e9, 1)},
         "roofline": roofline,
+        "workloads": workloads or None,
         "e2e": e2e,
-        "gpu_launches": step.launches_per_layer() * L * args.steps,
-        "clocks": clocks.summary(t0, t1),
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+    if leg is not None:
+        leg.fill(args.cpu_budget)
+        out["cpu_baseline"] = leg.baseline()
+        out["oracle_check"] = leg.checked
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def time_side_workload(dev, name: str, args, peak: float, sampler, leg):
+    """Time one more bandwidth-bound workload's store launches (a graph of
+    all its buffer copies, no epoch kernels) after checking its first copy
+    against the oracle; free its buffers afterwards."""
+    spec = SPECS[name]()
+    step = Step(dev, spec)
+    g = step.capture(with_epoch=False)
+    g.replay()
+    torch.cuda.synchronize()
+    checked = False
+    if leg is not None:
+        leg.check(f"{name}[copy 0]", spec.make(0), step.main[0], step.idx[0], spec.replicas,
+                  spec.num_blocks)
+        checked = True
+    store_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
+    store_ms = max_over_ranks(store_ms)
+    entry = roofline_entry(spec, step, store_ms, args.steps, peak, sampler.summary(t0, t1),
+                           checked)
+    del g, step
+    torch.cuda.empty_cache()
+    return entry
 
 
 # ------------------------------------------------------------- reference arm
@@ -549,12 +755,12 @@ def run_reference(args):
     slots = inputs.layer_slot_mapping()
     w = inputs.prefill_layer(0, slots)
     main, idx = oracle.new_caches(R, NUM_BLOCKS)
-    # size each step so warmup + steps take about two minutes in total
+    # size each step so warmup + steps take about --ref-seconds in total
     t = time.perf_counter()
     oracle.store_mla_fp8(w.kv_latent[:256], w.k_rope[:256], w.index_k[:256],
                          w.slot_mapping[:256], main, idx, NUM_BLOCKS)
     per_row = (time.perf_counter() - t) / 256
-    rows = int(min(ROWS, max(64, 120.0 / (args.steps + args.warmup) / per_row)))
+    rows = int(min(ROWS, max(64, args.ref_seconds / (args.steps + args.warmup) / per_row)))
     sample = slice(0, rows)
     valid = int(np.count_nonzero(w.slot_mapping[sample] >= 0))
     call = (w.kv_latent[sample], w.k_rope[sample], w.index_k[sample], w.slot_mapping[sample],
@@ -580,6 +786,22 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        return sock.getsockname()[1]
+
+
+def relaunch(n: int) -> int:
+    """Run this script again under torch.distributed.run with n local ranks
+    (one per GPU) and the same arguments; return its exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1",
+           "--master-port", str(free_port()), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -588,8 +810,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline field")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the CPU-baseline leg (and with it the oracle check)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the headline workload only")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="publish only the first K layers (a small profiling case)")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: about this many seconds of oracle work in all")
+    ap.add_argument("--write-traffic", metavar="CSV",
+                    help="write the roofline's DRAM traffic record from an ncu CSV and exit")
     ap.add_argument("--path", choices=["direct", "gather"], default="direct",
                     help="direct publication (the measured line) or the unfused "
                          "gather-then-insert path, for comparison")
@@ -597,9 +828,19 @@ def main():
                     help="the default is the measured line; the others are for "
                          "per-workload roofline figures and ncu captures")
     args = ap.parse_args()
+    if args.write_traffic:
+        print(json.dumps(write_traffic(args.write_traffic)))
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        raise SystemExit(relaunch(args.gpus))
     world, rank, local = dist_env()
+    if world != args.gpus and rank == 0:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {world}; using {world} ranks",
+              file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
         return

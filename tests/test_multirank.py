@@ -63,6 +63,21 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert res.stdout.strip() == ""
 
 
+def test_gpus_two_relaunches_under_torchrun_and_prints_one_line():
+    """--gpus 2 outside torchrun starts two local ranks; the reference arm
+    runs on rank 0 alone, so exactly one JSON line comes back, for 2 GPUs."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--gpus", "2", "--steps", "3", "--warmup", "3", "--ref-seconds", "1"],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
 def test_single_process_rate_is_units_over_time():
     sys.path.insert(0, ROOT)
     import bench
