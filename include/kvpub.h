@@ -127,6 +127,13 @@ typedef enum {
  *  num_blocks    >= 1.  block_size must be KVPUB_BLOCK_SIZE (64).
  *  invalid_count NULL, or a device uint64 counter. The call atomically adds
  *                the number of invalid (not -1, out-of-range) slots to it.
+ *
+ * Cache reads: no byte outside the written slots changes, but a launch of at
+ * least SMs x 8 tokens whose slots are not contiguous runs may read (into
+ * L2, never back to the caller) the 32-byte sectors that a written slot
+ * shares with its neighbours: the Main sector holding the slot's first or
+ * last 16 bytes, and the Indexer sector holding its scale. Those reads keep
+ * the partial sector writes from costing DRAM a read-modify-write each.
  */
 kvpub_status kvpub_store_mla_fp8(
     const void *kv_latent, int64_t latent_stride,
@@ -178,6 +185,12 @@ kvpub_status kvpub_store_mla_bf16(
  *              stays ready for the next call or graph replay. Calls that
  *              share one done_count must not run concurrently.
  *  Other arguments are as in kvpub_store_mla_fp8.
+ *
+ * This is the choice for eager (non-graph) loops, where the host's cost per
+ * launch dominates. Inside a CUDA graph, kvpub_store_mla_fp8 followed by
+ * kvpub_epoch_advance is faster: the graph removes the launch cost, and the
+ * separate one-thread epoch launch costs less than this kernel's end-of-grid
+ * counter round trip.
  */
 kvpub_status kvpub_store_mla_fp8_publish(
     const void *kv_latent, int64_t latent_stride,
