@@ -233,6 +233,51 @@ def test_byte_offsets_beyond_2_pow_31(dev):
     assert int((ixc[:(nb - 1) * 8448] != 0xA5).sum().item()) == 0
 
 
+def _mixed_batch():
+    """One batch of contiguous prefill runs interleaved, in chunks of 256 rows, with scattered
+    slots, some of them sharing a Main half-sector or an Indexer-scale sector with the end of a
+    run (each request's run ends at block offset 40, so offsets 41 and 43 are free), plus padded
+    and invalid entries."""
+    nb, R = 2048, 3
+    a = inputs.prefill_batch(901, 6, 1001, nb, R)
+    ends = a.slot_mapping.reshape(6, 1001)[:, -1]
+    shared = np.concatenate([ends + 1, ends + 3])
+    free = np.setdiff1d(np.arange(nb * 64), np.concatenate([a.slot_mapping, shared]))
+    rng = np.random.default_rng(902)
+    b_slots = np.concatenate([shared, rng.choice(free, 5988, replace=False)])
+    b = inputs.random_rows(903, b_slots.size, nb, R)
+    chunks_a = np.array_split(np.arange(a.num_tokens), a.num_tokens // 256)
+    chunks_b = np.array_split(np.arange(b_slots.size), b_slots.size // 256)
+    parts = []
+    for ca, cb in zip(chunks_a, chunks_b):
+        parts.append(("a", ca))
+        parts.append(("b", cb))
+    def take(name):
+        xa = getattr(a, name)
+        xb = b_slots if name == "slot_mapping" else getattr(b, name)
+        return np.concatenate([(xa if w == "a" else xb)[idx] for w, idx in parts])
+    slots = take("slot_mapping")
+    pad = rng.choice(slots.size, 70, replace=False)
+    slots[pad[:50]] = -1
+    slots[pad[50:]] = nb * 64 + np.arange(20) * 977
+    return workload("mixed", take("kv_latent"), take("k_rope"), take("index_k"), slots, R, nb)
+
+
+@pytest.mark.parametrize("path", ["fused", "publish", "gather"])
+def test_contiguous_runs_and_scattered_slots_in_one_launch(dev, path):
+    """Warps whose first row sits in a contiguous run leave the part-sector prefetch off, the
+    others turn it on; some scattered slots share a sector with a run's last row, so two warps
+    (one prefetching) write the two parts of one sector in the same launch."""
+    w = _mixed_batch()
+    assert w.num_tokens >= 8 * torch.cuda.get_device_properties(dev).multi_processor_count
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    c = run_store(w, dev, path, invalid_count=cnt)
+    want_main, want_idx, _, inv = oracle_caches(w)
+    assert inv == 20
+    assert_matches_oracle(c, want_main, want_idx)
+    assert int(cnt.item()) == inv
+
+
 def test_gather_equals_fused_on_prefill(dev):
     w = inputs.make(2)
     a = run_store(w, dev, "fused")
