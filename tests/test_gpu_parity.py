@@ -241,10 +241,13 @@ def _mixed_batch():
     nb, R = 2048, 3
     a = inputs.prefill_batch(901, 6, 1001, nb, R)
     ends = a.slot_mapping.reshape(6, 1001)[:, -1]
-    shared = np.concatenate([ends + 1, ends + 3])
+    # the cache's first and last slot too: their part-written sectors are the
+    # first and last ones of the buffers
+    edges = np.setdiff1d([0, 1, nb * 64 - 2, nb * 64 - 1], a.slot_mapping)
+    shared = np.concatenate([ends + 1, ends + 3, edges])
     free = np.setdiff1d(np.arange(nb * 64), np.concatenate([a.slot_mapping, shared]))
     rng = np.random.default_rng(902)
-    b_slots = np.concatenate([shared, rng.choice(free, 5988, replace=False)])
+    b_slots = np.concatenate([shared, rng.choice(free, 6000 - shared.size, replace=False)])
     b = inputs.random_rows(903, b_slots.size, nb, R)
     chunks_a = np.array_split(np.arange(a.num_tokens), a.num_tokens // 256)
     chunks_b = np.array_split(np.arange(b_slots.size), b_slots.size // 256)
