@@ -41,6 +41,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -114,11 +115,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with whitespace runs collapsed, so
+    that an edit to a comment does not count as a change of the kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the code the kernels are built from: every file under csrc/
+    and the public header (its layout constants are compiled in)."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(kbuild.CSRC)):
-        with open(os.path.join(kbuild.CSRC, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    paths = [os.path.join(kbuild.CSRC, n) for n in sorted(os.listdir(kbuild.CSRC))]
+    for path in paths + [os.path.join(kbuild.INCLUDE, "kvpub.h")]:
+        with open(path, encoding="utf-8") as f:
+            h.update(os.path.basename(path).encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -66,3 +66,11 @@ def test_committed_traffic_record_if_present_matches_its_command():
     rec = json.load(open(bench.TRAFFIC_JSON))
     assert rec["command"] == bench.TRAFFIC_CMD
     assert rec["launches"] == bench.TRAFFIC_LAYERS
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    a = "int x = 1; // one\n/* block\n comment */ int y =  2;\n"
+    b = "int x = 1;\nint y = 2; // edited comment\n"
+    c = "int x = 1;\nint y = 3;\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
