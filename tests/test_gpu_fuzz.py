@@ -2,7 +2,9 @@
 count, cache size, row strides, padding, invalid slots and value range, and
 runs one of the four store paths (direct, gather-then-insert, fused publish,
 bf16 cache) against the CPU oracle, byte for byte over every replica's whole
-buffer and its red zones.
+buffer and its red zones.  A second set draws only launches large enough for
+the kernel with the part-sector prefetch, mixing scattered slots with
+contiguous runs in caches 1.1x to 30x the batch.
 
 Each case also fills the row padding beyond the 512 / 64 / 128 used values
 with NaN bit patterns, so a kernel that read past a row's used columns would
@@ -79,7 +81,10 @@ def _strided(bits: np.ndarray, stride: int, dev) -> torch.Tensor:
 
 @pytest.mark.parametrize("seed", range(40))
 def test_random_case_matches_oracle(dev, seed):
-    c = _case(seed)
+    _run_case(dev, _case(seed), seed)
+
+
+def _run_case(dev, c, seed):
     T, R, nb, path = c["T"], c["R"], c["nb"], c["path"]
     bf16_cache = path == "bf16"
     main_bytes = nb * 64 * (1152 if bf16_cache else 656)
@@ -124,3 +129,48 @@ def test_random_case_matches_oracle(dev, seed):
         g = got.cpu().numpy()
         assert np.all(g[:RED] == 0xA5) and np.all(g[-RED:] == 0xA5), "red zone touched"
         assert np.array_equal(g[RED:-RED], want), f"case {seed}: T={T} R={R} nb={nb} {path}"
+
+
+def _large_case(seed):
+    """A launch of at least SMs x 8 rows (the instantiation with the part-sector
+    prefetch): the cache is 1.1x, 4x or 30x the batch, and each case mixes
+    scattered slots with contiguous runs of 64 to 1,024 slots, so some warps
+    take the prefetch and others do not."""
+    rng = np.random.default_rng(5000 + seed)
+    T = int(rng.integers(1216, 16385))
+    R = int(rng.integers(1, 9))
+    nb = int(-(-int(T * float(rng.choice([1.1, 4.0, 30.0]))) // 64))
+    cap = nb * 64
+    slots = np.empty(T, np.int64)
+    perm = rng.permutation(cap)
+    blocks = rng.permutation(nb)
+    used, t, bi, pi = set(), 0, 0, 0
+    while t < T:
+        if rng.random() < 0.5 and bi < nb:               # a contiguous run in a fresh block
+            run = int(min(T - t, rng.integers(64, 1025)))
+            start = int(blocks[bi]) * 64
+            bi += 1
+            cand = [s for s in range(start, min(start + run, cap)) if s not in used]
+        else:                                           # scattered slots
+            run = int(min(T - t, rng.integers(1, 257)))
+            cand = []
+            while len(cand) < run and pi < cap:
+                s = int(perm[pi])
+                pi += 1
+                if s not in used:
+                    cand.append(s)
+        cand = cand[:T - t]
+        if not cand:
+            cand = [int(s) for s in np.setdiff1d(np.arange(cap), list(used))[:T - t]]
+        used.update(cand)
+        slots[t:t + len(cand)] = cand
+        t += len(cand)
+    slots[rng.random(T) < 0.03] = -1
+    return dict(T=T, R=R, nb=nb, slots=slots, strides=(512, 64, 128),
+                lat=_values(rng, T, 512), rope=_values(rng, T, 64), idx=_values(rng, T, 128),
+                path=PATHS[seed % 3])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_large_mixed_case_matches_oracle(dev, seed):
+    _run_case(dev, _large_case(seed), seed)
