@@ -158,7 +158,9 @@ def read_ncu_csv(path: str, kernel: str = "store_mla_fp8_kernel"):
     import csv
     with open(path, newline="") as f:
         lines = f.read().splitlines()
-    start = next(i for i, l in enumerate(lines) if l.startswith('"ID"'))
+    start = next((i for i, l in enumerate(lines) if l.startswith('"ID"')), None)
+    if start is None:
+        raise SystemExit(f"{path}: no ncu --csv metrics table in it")
     launches = {}
     for row in csv.DictReader(lines[start:]):
         if kernel not in row["Kernel Name"]:

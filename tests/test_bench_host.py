@@ -74,3 +74,10 @@ def test_kernel_hash_ignores_comments_but_not_code():
     c = "int x = 1;\nint y = 3;\n"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_reader_refuses_a_file_without_a_metrics_table(tmp_path):
+    path = tmp_path / "empty.csv"
+    path.write_text("==PROF== Connected to process 1\n==ERROR== nothing profiled\n")
+    with pytest.raises(SystemExit, match="no ncu --csv metrics table"):
+        bench.read_ncu_csv(str(path))

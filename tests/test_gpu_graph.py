@@ -176,6 +176,42 @@ def test_two_dbo_lanes_on_two_streams_in_one_graph(dev):
             assert_matches_oracle(c, *oracle_caches(w)[:2])
 
 
+def test_scattered_slots_replay_in_a_graph(dev):
+    """The capacity batch (slots scattered over 706,624, so every warp takes
+    the part-sector prefetch) stored into two layers' caches, each store
+    followed by an epoch advance, captured once and replayed three times:
+    the epoch counts every replay and both layers equal the oracle."""
+    from gpu_util import DevInputs
+    w = inputs.make(4)
+    x = DevInputs(w, dev)
+    caches = [Caches(4, w.num_blocks, w.guard, dev) for _ in range(2)]
+    epoch = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def step():
+        for c in caches:
+            kvpub.store_mla_fp8(x.lat, x.rope, x.idx, x.slots, c.main, c.idx, w.num_blocks)
+            kvpub.epoch_advance(epoch)
+
+    step()
+    torch.cuda.synchronize()
+    epoch.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for c in caches:                       # replays must rewrite every byte
+        for b in c.main + c.idx:
+            b.fill_(w.guard)
+    for k in range(1, 4):
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(epoch.item()) == 2 * k
+    want_main, want_idx, _, _ = oracle_caches(w)
+    for c in caches:
+        assert_matches_oracle(c, want_main, want_idx)
+    del caches, x, g
+    torch.cuda.empty_cache()
+
+
 def test_bench_step_matches_oracle(dev):
     """The benchmark's own launch configuration: packed [T, 704] rows passed
     as strided views, one graph of 61 x (store + epoch advance), and the
