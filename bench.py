@@ -698,6 +698,7 @@ def run_ours(args):
             workloads[WORKLOAD] = roofline_entry(spec, step, store_ms, args.steps, peak,
                                                  store_clocks, oracle_checked)
         launches_per_step = step.launches_per_layer() * L
+        rows_per_layer, valid_per_layer = step.num_tokens, step.valid[0]
         l2_note = ("inputs larger than L2: one step touches "
                    f"{sum(launch_bytes) / 1e9:.2f} GB")
         del g, g_store, step
@@ -711,9 +712,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": spec.name, "layers": L, "rows_per_layer": ROWS
-                   if spec.name == WORKLOAD else None,
-                   "replicas": Rr, "blocks_per_replica": spec.num_blocks,
+        "config": {"workload": spec.name, "layers": L, "rows_per_layer": rows_per_layer,
+                   "valid_rows_per_layer": valid_per_layer, "replicas": Rr, "blocks_per_replica": spec.num_blocks,
                    "launches_per_step": launches_per_step, "path": args.path,
                    "graph": True, "parallelism": f"replicas only x{world}", "note": spec.note,
                    "direct_equals_gather_before_timing": checked,
