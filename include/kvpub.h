@@ -61,6 +61,15 @@
  * every one of the num_tokens input rows must be readable. Slots must be
  * distinct. If two tokens name the same slot, the bytes left there are
  * unspecified.
+ *
+ * Cache reads: no byte outside the written slots changes. An fp8 store
+ * launch of at least SMs x 8 tokens whose slots are not contiguous runs
+ * (kvpub_store_mla_fp8, kvpub_store_mla_fp8_publish, and the inserts of the
+ * gather-then-insert calls) may read, into L2 and never back to the caller,
+ * the 32-byte sectors that a written slot shares with its neighbours: the
+ * Main sector holding the slot's first or last 16 bytes, and the Indexer
+ * sector holding its scale. Those reads keep each partial sector write from
+ * costing DRAM a read-modify-write.
  */
 #ifndef KVPUB_H
 #define KVPUB_H
@@ -127,13 +136,7 @@ typedef enum {
  *  num_blocks    >= 1.  block_size must be KVPUB_BLOCK_SIZE (64).
  *  invalid_count NULL, or a device uint64 counter. The call atomically adds
  *                the number of invalid (not -1, out-of-range) slots to it.
- *
- * Cache reads: no byte outside the written slots changes, but a launch of at
- * least SMs x 8 tokens whose slots are not contiguous runs may read (into
- * L2, never back to the caller) the 32-byte sectors that a written slot
- * shares with its neighbours: the Main sector holding the slot's first or
- * last 16 bytes, and the Indexer sector holding its scale. Those reads keep
- * the partial sector writes from costing DRAM a read-modify-write each.
+
  */
 kvpub_status kvpub_store_mla_fp8(
     const void *kv_latent, int64_t latent_stride,
