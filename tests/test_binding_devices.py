@@ -28,10 +28,10 @@ def test_store_arguments_are_checked_against_the_current_device(monkeypatch):
     set by hand."""
 
     class FakeTensor:
-        def __init__(self, device, dtype, shape, stride=None):
+        def __init__(self, device, dtype, shape):
             self.device = torch.device(device)
             self.dtype, self.shape = dtype, shape
-            self._stride = stride or (shape[1], 1) if len(shape) == 2 else (1,)
+            self._stride = (shape[1], 1) if len(shape) == 2 else (1,)
             self.is_cuda = self.device.type == "cuda"
 
         def dim(self):
