@@ -17,6 +17,11 @@ this c4 x 3,584 prefill and the 706,624-slot capacity batch.  Before any
 timing, the timed buffers are compared byte for byte with the oracle's.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--path direct|publish|gather] [--workload NAME]
+
+--path publish times the same step with the store and the epoch advance
+fused into one launch per layer; --path gather the unfused
+gather-then-insert path.
 
 With --gpus N > 1 outside torchrun, the script starts itself again under
 torch.distributed.run with N local ranks (one per GPU).
@@ -351,8 +356,11 @@ class Step:
         if path == "gather":
             self.workspace = torch.empty(kvpub.gather_workspace_bytes(T), dtype=torch.uint8,
                                          device=dev)
+        self.done = torch.zeros(1, dtype=torch.int32, device=dev)     # publish path only
 
     def launches_per_layer(self, with_epoch: bool = True) -> int:
+        if self.path == "publish":
+            return 1                        # the store advances the epoch itself
         n = 1 + self.spec.replicas if self.path == "gather" else 1
         return n + (1 if with_epoch else 0)
 
@@ -365,7 +373,14 @@ class Step:
             self.launch_layer(layer, with_epoch)
 
     def launch_layer(self, layer: int, with_epoch: bool = True):
+        """One layer's publication.  On the publish path the single fused
+        launch stores and advances the epoch, whatever with_epoch says."""
         lat, rope, idx = self.views(layer)
+        if self.path == "publish":
+            kvpub.store_mla_fp8_publish(lat, rope, idx, self.slots[layer], self.main[layer],
+                                        self.idx[layer], self.epoch, self.done,
+                                        self.spec.num_blocks, invalid_count=self.invalid)
+            return
         if self.path == "gather":
             kvpub.gather_insert(lat, rope, idx, self.slots[layer], self.main[layer],
                                 self.idx[layer], self.workspace, self.spec.num_blocks,
@@ -622,8 +637,8 @@ def run_ours(args):
             raise SystemExit(f"--layers must be in 1..{spec.layers}")
         spec.layers = args.layers
         spec.note += f" (first {args.layers} layers only)"
-    if args.path == "gather" and spec.bf16_cache:
-        raise SystemExit("the gather-then-insert path exists for the fp8 cache only")
+    if args.path != "direct" and spec.bf16_cache:
+        raise SystemExit(f"the {args.path} path exists for the fp8 cache only")
     leg = OracleLeg() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     step = Step(dev, spec, args.path)
     L, Rr = spec.layers, spec.replicas
@@ -634,31 +649,36 @@ def run_ours(args):
     g.replay()
     torch.cuda.synchronize()
     oracle_checked = False
-    if leg is not None and spec.name == WORKLOAD and args.path == "direct":
+    if leg is not None and spec.name == WORKLOAD and args.path in ("direct", "publish"):
         for layer in sorted({0, L - 1}):
             w = spec.make(layer)
             leg.check(f"{WORKLOAD}[{layer}]", w, step.main[layer], step.idx[layer], Rr,
                       spec.num_blocks, headline_layer=layer)
         oracle_checked = True
     peak, peak_kind = measured_peak()
+    epoch_before = int(step.epoch.item())
     with ClockSampler(local) as sampler:
         total_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
+        epoch_after = int(step.epoch.item())
         store_ms, s0, s1 = time_graph(g_store, args.steps, args.warmup)
         clocks = sampler.summary(t0, t1)
         store_clocks = sampler.summary(s0, s1)
         total_ms = max_over_ranks(total_ms)
         store_ms = max_over_ranks(store_ms)
         ms_per_step = total_ms / args.steps
-        expected_epoch = L * (1 + args.warmup + args.steps)
-        epoch = int(step.epoch.item())
-        if epoch != expected_epoch:
-            raise RuntimeError(f"epoch {epoch} != {expected_epoch}: launches were lost")
+        expected = L * (args.warmup + args.steps)
+        if epoch_after - epoch_before != expected:
+            raise RuntimeError(f"the epoch advanced by {epoch_after - epoch_before} over the "
+                               f"timed replays, not {expected}: launches were lost")
 
         rows_x_r = sum(step.valid) * Rr
         value = whole_job_rate(world, rows_x_r, ms_per_step)
         if args.path == "gather":
             launch_bytes = [gather_insert_bytes(step.num_tokens, v, Rr) for v in step.valid]
             kernel_name = f"gather_rows_kernel + {Rr} x store_mla_fp8_kernel<1> (per layer)"
+        elif args.path == "publish":
+            launch_bytes = [store_bytes(step.num_tokens, v, Rr) for v in step.valid]
+            kernel_name = f"store_mla_fp8_publish_kernel<{Rr}>"
         else:
             launch_bytes = [store_bytes(step.num_tokens, v, Rr, spec.bf16_cache)
                             for v in step.valid]
@@ -666,7 +686,8 @@ def run_ours(args):
         per_launch = sum(launch_bytes) / L
         kernel_ms = store_ms / (args.steps * L)
         timing = (f"CUDA events around {args.steps} replays of a graph of the same {L} layers' "
-                  f"store launches (no epoch kernels) / {args.steps * L} layers, gaps included")
+                  f"store launches (no separate epoch kernels) / {args.steps * L} layers, "
+                  "gaps included")
         achieved = per_launch / (kernel_ms / 1e3) / 1e9
         traffic = (profiled_traffic() if (spec.name == WORKLOAD and args.path == "direct")
                    else None)
@@ -835,8 +856,9 @@ def main():
                     help="--impl reference: about this many seconds of oracle work in all")
     ap.add_argument("--write-traffic", metavar="CSV",
                     help="write the roofline's DRAM traffic record from an ncu CSV and exit")
-    ap.add_argument("--path", choices=["direct", "gather"], default="direct",
-                    help="direct publication (the measured line) or the unfused "
+    ap.add_argument("--path", choices=["direct", "publish", "gather"], default="direct",
+                    help="direct publication with a separate epoch launch (the measured "
+                         "line), the store + epoch fused in one launch, or the unfused "
                          "gather-then-insert path, for comparison")
     ap.add_argument("--workload", choices=sorted(SPECS), default=WORKLOAD,
                     help="the default is the measured line; the others are for "

@@ -250,6 +250,31 @@ def test_bench_step_matches_oracle(dev):
     torch.cuda.empty_cache()
 
 
+def test_bench_publish_path_matches_oracle(dev):
+    """The benchmark's fused path: one store + epoch launch per layer in one
+    graph; one replay advances the epoch by 61 and layers 0 and 60 equal the
+    oracle."""
+    import bench
+
+    step = bench.Step(dev, bench.SPECS[bench.WORKLOAD](), "publish")
+    assert step.launches_per_layer() == 1
+    g = step.capture(with_epoch=True)
+    torch.cuda.synchronize()
+    before = int(step.epoch.item())
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(step.epoch.item()) == before + LAYERS
+    assert int(step.done.item()) == 0
+    slots = inputs.layer_slot_mapping()
+    for layer in (0, 60):
+        want_main, want_idx, _, _ = oracle_caches(inputs.prefill_layer(layer, slots))
+        for r in range(4):
+            assert np.array_equal(step.main[layer][r].cpu().numpy(), want_main[r])
+            assert np.array_equal(step.idx[layer][r].cpu().numpy(), want_idx[r])
+    del step, g
+    torch.cuda.empty_cache()
+
+
 def test_every_capturable_call_replays_in_a_graph(dev):
     """gather-then-insert, the bf16 store and the bounded wait, captured with
     the epoch advance and replayed twice: bytes as the oracle's, epoch and
