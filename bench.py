@@ -21,7 +21,8 @@ timing, the timed buffers are compared byte for byte with the oracle's.
 
 --path publish times the same step with the store and the epoch advance
 fused into one launch per layer; --path gather the unfused
-gather-then-insert path.
+gather-then-insert path.  --eager issues the step's calls one by one from
+the host (arguments marshalled once) instead of replaying a graph.
 
 With --gpus N > 1 outside torchrun, the script starts itself again under
 torch.distributed.run with N local ranks (one per GPU).
@@ -392,6 +393,25 @@ class Step:
         if with_epoch:
             kvpub.epoch_advance(self.epoch)
 
+    def prepared_calls(self):
+        """Every layer's calls with their arguments marshalled once (for an
+        eager loop): store + epoch advance, or the fused store + epoch."""
+        if self.path == "gather" or self.spec.bf16_cache:
+            raise SystemExit("--eager times the direct and publish paths of the fp8 cache")
+        calls = []
+        for layer in range(self.spec.layers):
+            lat, rope, idx = self.views(layer)
+            args = (lat, rope, idx, self.slots[layer], self.main[layer], self.idx[layer])
+            if self.path == "publish":
+                calls.append(kvpub.prepare_store_mla_fp8_publish(
+                    *args, self.epoch, self.done, self.spec.num_blocks,
+                    invalid_count=self.invalid))
+            else:
+                calls.append(kvpub.prepare_store_mla_fp8(
+                    *args, self.spec.num_blocks, invalid_count=self.invalid))
+                calls.append(kvpub.prepare_epoch_advance(self.epoch))
+        return calls
+
     def capture(self, with_epoch: bool = True):
         """One graph of all layers: store (+ epoch advance) per layer."""
         self.launch_layers(with_epoch=False)    # load the kernels before capture
@@ -465,6 +485,31 @@ def time_graph(g, steps, warmup):
     start.record()
     for _ in range(steps):
         g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    barrier()
+    return start.elapsed_time(end), t0, t1
+
+
+def time_eager(calls, steps, warmup):
+    """K steps of the calls issued one by one from the host (no graph), with
+    CUDA events around them: the host's cost per call shows in the time.
+    Each call gets the current stream's raw handle, looked up once."""
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(warmup):
+        for c in calls:
+            c(stream)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    start.record()
+    for _ in range(steps):
+        for c in calls:
+            c(stream)
     end.record()
     torch.cuda.synchronize()
     t1 = time.monotonic()
@@ -658,7 +703,10 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     epoch_before = int(step.epoch.item())
     with ClockSampler(local) as sampler:
-        total_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
+        if args.eager:
+            total_ms, t0, t1 = time_eager(step.prepared_calls(), args.steps, args.warmup)
+        else:
+            total_ms, t0, t1 = time_graph(g, args.steps, args.warmup)
         epoch_after = int(step.epoch.item())
         store_ms, s0, s1 = time_graph(g_store, args.steps, args.warmup)
         clocks = sampler.summary(t0, t1)
@@ -736,7 +784,8 @@ def run_ours(args):
         "config": {"workload": spec.name, "layers": L, "rows_per_layer": rows_per_layer,
                    "valid_rows_per_layer": valid_per_layer, "replicas": Rr, "blocks_per_replica": spec.num_blocks,
                    "launches_per_step": launches_per_step, "path": args.path,
-                   "graph": True, "parallelism": f"replicas only x{world}", "note": spec.note,
+                   "graph": not args.eager,
+                   "parallelism": f"replicas only x{world}", "note": spec.note,
                    "direct_equals_gather_before_timing": checked,
                    "oracle_checked_before_timing": oracle_checked,
                    "l2": l2_note,
@@ -860,6 +909,9 @@ def main():
                     help="direct publication with a separate epoch launch (the measured "
                          "line), the store + epoch fused in one launch, or the unfused "
                          "gather-then-insert path, for comparison")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the step as calls issued one by one from the host, "
+                         "arguments marshalled once, instead of a CUDA graph replay")
     ap.add_argument("--workload", choices=sorted(SPECS), default=WORKLOAD,
                     help="the default is the measured line; the others are for "
                          "per-workload roofline figures and ncu captures")

@@ -121,13 +121,16 @@ def _current_device() -> int:
     return torch.cuda.current_device()
 
 
-def _stream_handle(stream, current: int | None = None) -> int:
+def _stream_handle(stream, device: int) -> int:
     """The raw cudaStream_t to launch on: the current torch stream by
-    default.  A torch.cuda.Stream must belong to the current device."""
+    default.  A torch.cuda.Stream must belong to ``device``, the device the
+    call's tensors were checked against (a raw handle is passed as is)."""
     if stream is None:
         stream = torch.cuda.current_stream()
     if isinstance(stream, torch.cuda.Stream):
-        check_devices([stream.device], _current_device() if current is None else current)
+        if stream.device_index != device:
+            raise ValueError(f"stream of cuda:{stream.device_index} for tensors on the current "
+                             f"CUDA device cuda:{device}: call under torch.cuda.device(...)")
         return stream.cuda_stream
     return int(stream)
 
@@ -225,7 +228,7 @@ def store_mla_fp8(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer
         _check_distinct(slot_mapping, main_caches, num_blocks)
     args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
                        num_blocks, invalid_count)
-    check(lib().kvpub_store_mla_fp8(*args, _stream_handle(stream)))
+    check(lib().kvpub_store_mla_fp8(*args, _stream_handle(stream, _current_device())))
 
 
 def store_mla_bf16(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
@@ -234,7 +237,7 @@ def store_mla_bf16(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexe
     (Main slot 1152 B, Indexer slot 256 B)."""
     args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
                        num_blocks, invalid_count, bf16_cache=True)
-    check(lib().kvpub_store_mla_bf16(*args, _stream_handle(stream)))
+    check(lib().kvpub_store_mla_bf16(*args, _stream_handle(stream, _current_device())))
 
 
 def store_mla_fp8_publish(kv_latent, k_rope, index_k, slot_mapping, main_caches,
@@ -246,7 +249,7 @@ def store_mla_fp8_publish(kv_latent, k_rope, index_k, slot_mapping, main_caches,
     _counter(epoch, (torch.int64, torch.uint64), "epoch")
     _counter(done_count, (torch.int32, torch.uint32), "done_count")
     check(lib().kvpub_store_mla_fp8_publish(*args, epoch.data_ptr(), done_count.data_ptr(),
-                                            _stream_handle(stream)))
+                                            _stream_handle(stream, _current_device())))
 
 
 def gather_workspace_bytes(num_tokens: int) -> int:
@@ -263,7 +266,7 @@ def gather_insert(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer
     check_devices([workspace.device], _current_device())
     nbytes = workspace.numel() * workspace.element_size()
     check(lib().kvpub_gather_insert(*args, workspace.data_ptr(), nbytes,
-                                    _stream_handle(stream)))
+                                    _stream_handle(stream, _current_device())))
 
 
 def gather_insert_noalloc(kv_latent, k_rope, index_k, slot_mapping, main_caches,
@@ -274,24 +277,29 @@ def gather_insert_noalloc(kv_latent, k_rope, index_k, slot_mapping, main_caches,
     calls that overlap on the GPU race on the shared workspace)."""
     args = _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_caches,
                        num_blocks, invalid_count)
-    check(lib().kvpub_gather_insert_noalloc(*args, _stream_handle(stream)))
+    check(lib().kvpub_gather_insert_noalloc(*args,
+                                            _stream_handle(stream, _current_device())))
 
 
 class PreparedCall:
     """One library call with its arguments marshalled once (shapes checked,
     pointers and the replica pointer arrays built).  Calling it passes only
     the stream, which cuts the per-call host cost of an eager (non-graph)
-    serving loop.  It keeps the tensors it was prepared with alive; they must
-    not be reallocated while it is in use."""
+    serving loop.  The cheapest form passes the raw cudaStream_t handle
+    (``torch.cuda.current_stream().cuda_stream``, looked up once per loop):
+    with no stream, each call looks up torch's current stream, which costs
+    a few microseconds.  It keeps the tensors it was prepared with alive;
+    they must not be reallocated while it is in use."""
 
     def __init__(self, fn, args, keep):
         self._fn, self._args, self._keep = fn, tuple(args), keep
         self._device = _current_device()
 
     def __call__(self, stream=None) -> None:
-        current = _current_device()
-        check_devices([torch.device("cuda", self._device)], current)
-        check(self._fn(*self._args, _stream_handle(stream, current)))
+        # The default stream is the current device's: if the current device
+        # is no longer the one the tensors were checked on, its device index
+        # differs and the call is refused (one integer comparison).
+        check(self._fn(*self._args, _stream_handle(stream, self._device)))
 
 
 def prepare_store_mla_fp8(kv_latent, k_rope, index_k, slot_mapping, main_caches,
@@ -333,7 +341,8 @@ def _counter(t, dtypes, name):
 def epoch_advance(epoch: torch.Tensor, stream=None) -> None:
     """Release all earlier stores on the stream, then add 1 to ``epoch``."""
     _counter(epoch, (torch.int64, torch.uint64), "epoch")
-    check(lib().kvpub_epoch_advance(epoch.data_ptr(), _stream_handle(stream)))
+    check(lib().kvpub_epoch_advance(epoch.data_ptr(),
+                                    _stream_handle(stream, _current_device())))
 
 
 def epoch_wait(epoch: torch.Tensor, target: int, max_polls: int, status: torch.Tensor,
@@ -342,4 +351,4 @@ def epoch_wait(epoch: torch.Tensor, target: int, max_polls: int, status: torch.T
     _counter(epoch, (torch.int64, torch.uint64), "epoch")
     _counter(status, (torch.int32, torch.uint32), "status")
     check(lib().kvpub_epoch_wait(epoch.data_ptr(), int(target), int(max_polls),
-                                 status.data_ptr(), _stream_handle(stream)))
+                                 status.data_ptr(), _stream_handle(stream, _current_device())))
