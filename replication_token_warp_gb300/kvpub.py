@@ -110,11 +110,18 @@ def check_devices(devices, current: int) -> None:
     """Raise ValueError unless every device in ``devices`` is CUDA device
     ``current``.  The library launches on the calling thread's current
     device and dereferences every pointer there, so a tensor (or stream) of
-    another GPU would make a kernel touch memory it cannot address."""
+    another GPU would make a kernel touch memory it cannot address.  A
+    device is a torch.device or a CUDA device index (``Tensor.get_device()``,
+    -1 for a CPU tensor)."""
     for d in devices:
-        if d.type != "cuda" or d.index != current:
-            raise ValueError(f"{d} is not the current CUDA device cuda:{current}: call "
-                             "under torch.cuda.device(...) of the tensors' device")
+        if isinstance(d, int):
+            if d == current:
+                continue
+            d = torch.device("cuda", d) if d >= 0 else torch.device("cpu")
+        elif d.type == "cuda" and d.index == current:
+            continue
+        raise ValueError(f"{d} is not the current CUDA device cuda:{current}: call "
+                         "under torch.cuda.device(...) of the tensors' device")
 
 
 def _current_device() -> int:
@@ -189,7 +196,7 @@ def _store_args(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer_c
     tensors = [kv_latent, k_rope, index_k, slot_mapping, *main_caches, *indexer_caches]
     if invalid_count is not None:
         tensors.append(invalid_count)
-    check_devices([t.device for t in tensors], _current_device())
+    check_devices([t.get_device() for t in tensors], _current_device())
     return [lp, ls, rp, rs, ip, is_, slot_mapping.data_ptr(), T, mains, idxs,
             len(main_caches), nb, BLOCK_SIZE, cnt]
 
@@ -263,7 +270,7 @@ def gather_insert(kv_latent, k_rope, index_k, slot_mapping, main_caches, indexer
                        num_blocks, invalid_count)
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace: expected a contiguous CUDA tensor")
-    check_devices([workspace.device], _current_device())
+    check_devices([workspace.get_device()], _current_device())
     nbytes = workspace.numel() * workspace.element_size()
     check(lib().kvpub_gather_insert(*args, workspace.data_ptr(), nbytes,
                                     _stream_handle(stream, _current_device())))
@@ -335,7 +342,7 @@ def prepare_epoch_advance(epoch) -> PreparedCall:
 def _counter(t, dtypes, name):
     if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in dtypes or t.numel() < 1:
         raise ValueError(f"{name}: expected a CUDA tensor of {dtypes}")
-    check_devices([t.device], _current_device())
+    check_devices([t.get_device()], _current_device())
 
 
 def epoch_advance(epoch: torch.Tensor, stream=None) -> None:

@@ -22,6 +22,14 @@ def test_other_devices_are_refused(dev):
         kvpub.check_devices([torch.device("cuda", 0), dev], 0)
 
 
+def test_device_indices_are_accepted_too():
+    kvpub.check_devices([0, 0, torch.device("cuda", 0)], 0)
+    with pytest.raises(ValueError, match="cuda:2 is not the current CUDA device cuda:0"):
+        kvpub.check_devices([0, 2], 0)
+    with pytest.raises(ValueError, match="cpu is not the current CUDA device"):
+        kvpub.check_devices([-1], 0)
+
+
 def test_store_arguments_are_checked_against_the_current_device(monkeypatch):
     """_store_args compares every tensor's device with the current one; on a
     machine without a GPU this runs with stand-in tensors whose devices are
@@ -33,6 +41,9 @@ def test_store_arguments_are_checked_against_the_current_device(monkeypatch):
             self.dtype, self.shape = dtype, shape
             self._stride = (shape[1], 1) if len(shape) == 2 else (1,)
             self.is_cuda = self.device.type == "cuda"
+
+        def get_device(self):
+            return self.device.index if self.device.type == "cuda" else -1
 
         def dim(self):
             return len(self.shape)
