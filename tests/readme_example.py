@@ -1,4 +1,4 @@
-"""The library's Python usage example, as the readme shows it.
+"""The library's Python usage example, as its front-page documentation shows it.
 
 Publishes 1,024 token rows into 4 replicas of a 256-block fp8 cache, then
 advances the device epoch.  tests/test_gpu_readme.py runs this file and

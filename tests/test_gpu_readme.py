@@ -1,5 +1,5 @@
 """The repository's Python usage example (tests/readme_example.py, shown in
-the readme) runs as written, and every slot it writes holds the bytes the
+the front-page documentation) runs as written, and every slot it writes holds the bytes the
 CPU oracle computes from the example's own inputs.  The example's caches
 start uninitialised, so only the written slots are compared; the
 whole-buffer checks are in test_gpu_parity.py."""
