@@ -682,6 +682,11 @@ def run_ours(args):
             raise SystemExit(f"--layers must be in 1..{spec.layers}")
         spec.layers = args.layers
         spec.note += f" (first {args.layers} layers only)"
+    if args.replicas is not None:
+        if not 1 <= args.replicas <= kvpub.MAX_REPLICAS:
+            raise SystemExit(f"--replicas must be in 1..{kvpub.MAX_REPLICAS}")
+        spec.replicas = args.replicas
+        spec.note += f" ({args.replicas} replicas)"
     if args.path != "direct" and spec.bf16_cache:
         raise SystemExit(f"the {args.path} path exists for the fp8 cache only")
     leg = OracleLeg() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
@@ -737,8 +742,8 @@ def run_ours(args):
                   f"store launches (no separate epoch kernels) / {args.steps * L} layers, "
                   "gaps included")
         achieved = per_launch / (kernel_ms / 1e3) / 1e9
-        traffic = (profiled_traffic() if (spec.name == WORKLOAD and args.path == "direct")
-                   else None)
+        traffic = (profiled_traffic()
+                   if (spec.name == WORKLOAD and args.path == "direct" and Rr == R) else None)
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                     "kernel": kernel_name, "algorithmic_bytes": int(round(per_launch)),
@@ -901,6 +906,8 @@ def main():
                     help="time the headline workload only")
     ap.add_argument("--layers", type=int, default=None,
                     help="publish only the first K layers (a small profiling case)")
+    ap.add_argument("--replicas", type=int, default=None,
+                    help="store into R replicas instead of the workload's own count")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: about this many seconds of oracle work in all")
     ap.add_argument("--write-traffic", metavar="CSV",
