@@ -22,6 +22,15 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 constexpr int kThreads = kWarpsPerBlock * 32;
+// The row loop is tuned for 4 resident blocks of kThreads threads per SM,
+// which needs at most 64 registers a thread.  The compiler gets there by
+// itself for most instantiations.  The few it would give more registers
+// (3 blocks per SM) are held to it explicitly: the bf16 store with one
+// replica and the fused publish with two or three, each 3-4 % faster so.
+// A minimum of 0 blocks leaves the choice to the compiler (an explicit 1
+// would let it spend up to 255 registers).
+template <int R> constexpr int kBf16MinBlocks = (R == 1) ? 4 : 0;
+template <int R> constexpr int kPublishMinBlocks = (R == 2 || R == 3) ? 4 : 0;
 // Block size of a launch too small to give every SM a block of kWarpsPerBlock rows.
 constexpr int kSmallBlockWarps = 2;
 constexpr unsigned long long kMaxPolls = KVPUB_MAX_POLLS;
@@ -280,7 +289,8 @@ __global__ void __launch_bounds__(kThreads) store_mla_fp8_kernel(const StoreArgs
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads) store_mla_bf16_kernel(const StoreArgs a) {
+__global__ void __launch_bounds__(kThreads, kBf16MinBlocks<R>)
+store_mla_bf16_kernel(const StoreArgs a) {
     wait_previous_kernel();
     publish_rows<R, false, false>(a);
 }
@@ -291,7 +301,7 @@ __device__ __forceinline__ void release_add_epoch(unsigned long long *epoch) {
 
 // Store, then the last block to finish publishes the epoch.
 template <int R, bool kPrefetch>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kPublishMinBlocks<R>)
 store_mla_fp8_publish_kernel(const StoreArgs a, unsigned long long *epoch,
                              unsigned int *done_count) {
     wait_previous_kernel();
