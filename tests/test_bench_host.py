@@ -81,3 +81,30 @@ def test_reader_refuses_a_file_without_a_metrics_table(tmp_path):
     path.write_text("==PROF== Connected to process 1\n==ERROR== nothing profiled\n")
     with pytest.raises(SystemExit, match="no ncu --csv metrics table"):
         bench.read_ncu_csv(str(path))
+
+
+def test_oracle_leg_checks_every_byte_and_times_headline_layers_only():
+    """The bench's pre-timing check: buffers equal to the oracle's bytes pass,
+    one flipped byte anywhere raises; only headline layers count toward the
+    CPU baseline."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from replication_token_warp_gb300 import inputs
+
+    w = inputs.make(0)
+    main, idx = oracle.new_caches(w.num_replicas, w.num_blocks, inputs.GUARD_BYTE)
+    oracle.store_mla_fp8(w.kv_latent, w.k_rope, w.index_k, w.slot_mapping, main, idx,
+                         w.num_blocks)
+    got_main = [torch.from_numpy(m.copy()) for m in main]
+    got_idx = [torch.from_numpy(x.copy()) for x in idx]
+    leg = bench.OracleLeg()
+    leg.check("tiny", w, got_main, got_idx, w.num_replicas, w.num_blocks)
+    assert leg.row_replicas == 0 and leg.layers == []
+    leg.check("tiny as layer 5", w, got_main, got_idx, w.num_replicas, w.num_blocks,
+              headline_layer=5)
+    assert leg.layers == [5] and leg.row_replicas == w.num_valid * w.num_replicas
+    got_idx[0][int(np.flatnonzero(idx[0] != inputs.GUARD_BYTE)[-1])] ^= 1
+    with pytest.raises(RuntimeError, match="Indexer cache of replica 0 differs"):
+        leg.check("tiny", w, got_main, got_idx, w.num_replicas, w.num_blocks)
